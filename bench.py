@@ -1,0 +1,373 @@
+#!/usr/bin/env python3
+"""Benchmark of the Hadamard-folded 1-bit GEMV (decode tokens/s and weight GB/s).
+
+One step = one bitlin_forward call: M tokens through one folded one-bit
+matrix (default: the ffn_gate shape, M=1, K=5120, N=17408).  Consecutive steps
+cycle through R distinct copies of the matrix whose total size is at least
+four times the L2 cache, so every step streams its weights from HBM.  Steps
+are replayed from CUDA graphs; the timed region is bracketed by a barrier and
+a device synchronize, timed with CUDA events on the launching stream, and the
+max over ranks is reported.
+
+--impl reference times the CPU oracle (the plain f64 definition) on the
+host's cores instead, in row chunks sized so the whole run ends within a few
+minutes; its tokens/s counts the fraction of a token each chunk completes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "decode tokens/s and weight GB/s (% of HBM peak), 1-bit WHT GEMV K=5120 N=17408"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="ffn_gate")
+    ap.add_argument("--M", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0)
+    ap.add_argument("--e2e-steps", type=int, default=20000)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_record(kernel: str, workload: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if it still matches the kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(f"{kernel}:{workload}")
+    if not entry:
+        return None
+    src = os.path.join(ROOT, "hadamard_rotated_binary_gb300", "csrc", entry["source"])
+    try:
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    return entry["bytes_per_launch"] if digest == entry["sha256"] else None
+
+
+def cpu_baseline(w: synth.Workload, inputs, seconds: float):
+    """The oracle, as it stands, on the host cores: whole calls for about `seconds`."""
+    import oracle
+
+    oracle.build()
+    bits, scales, signs, x = inputs
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.forward(bits, scales, signs, w.perm, x)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": n * w.M / el, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{n} whole oracle calls (M={w.M}, K={w.K}, N={w.N}) in {el:.1f} s, "
+                      f"f64, OpenMP over output rows"}
+
+
+def run_reference(args, w: synth.Workload):
+    """Reference arm: the CPU oracle on this workload, in bounded row chunks."""
+    import oracle
+
+    oracle.build()
+    bits, scales, signs, x = synth.make_inputs(w)
+    # Calibrate: one rotation and one chunk of 256 rows.
+    t0 = time.perf_counter()
+    xt = oracle.rotate(x, signs, w.perm)
+    t_rot = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.product(bits, scales, xt, np.arange(min(256, w.N)))
+    t_row = (time.perf_counter() - t0) / min(256, w.N)
+    total_steps = args.steps + args.warmup
+    per_step = args.ref_seconds / max(total_steps, 1)
+    # rows per step so that rows * t_row plus the rotation's share fits per_step
+    rows = int(max(1, min(w.N, per_step / max(t_row, 1e-9))))
+    while rows > 1 and rows * t_row + t_rot * rows / w.N > per_step:
+        rows = max(1, rows // 2)
+    # A step computes `rows` output rows of the current token; the token's
+    # rotation is computed at its first chunk and reused by the rest of it.
+    chunks_per_token = (w.N + rows - 1) // rows
+    state = {"i": 0, "xt": None}
+
+    def step():
+        c = state["i"] % chunks_per_token
+        if c == 0 or state["xt"] is None:
+            state["xt"] = oracle.rotate(x, signs, w.perm)
+        lo = c * rows
+        r = np.arange(lo, min(w.N, lo + rows))
+        oracle.product(bits, scales, state["xt"], r)
+        state["i"] += 1
+        return r.size
+
+    for _ in range(args.warmup):
+        step()
+    state["i"] = 0
+    done = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        done += step()
+    el = time.perf_counter() - t0
+    tokens = w.M * done / w.N
+    value = tokens / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / max(args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64: Bernoulli(0.5) bits, U[0.005,0.03] fp16 scales, +-1 signs, N(0,1) x)",
+        "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "perm": w.perm,
+                   "rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": f"{args.steps} steps of {rows} output rows each (rotation once per token)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    w = synth.workload(args.workload, args.M)
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w)
+        return
+
+    import torch
+
+    torch.cuda.set_device(local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+
+    import hadamard_rotated_binary_gb300 as hrb
+    from hadamard_rotated_binary_gb300 import build as hbuild
+
+    hbuild.build()
+    dev = torch.device("cuda", local)
+    inputs = synth.make_inputs(w)
+    bits, scales, signs, x = inputs
+    tb = torch.from_numpy(bits.view(np.int32)).to(dev)
+    ts = torch.from_numpy(scales.view(np.int16)).to(dev)
+    tg = torch.from_numpy(signs).to(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    wbytes = w.weight_bytes()
+    R = max(2, -(-4 * l2 // wbytes))
+    layers = [hrb.BitLinear(tb, ts, tg, w.perm) for _ in range(R)]
+    del tb, ts, tg
+    xd = torch.from_numpy(x).to(dev)
+    yd = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+
+    stream = torch.cuda.Stream(device=dev)
+    # Warm-up (also allocates every handle's scratch before capture).
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, R)):
+            layers[i % R](xd, out=yd, stream=stream)
+    stream.synchronize()
+
+    chunk = R * max(1, 256 // R)
+    def capture(ncalls):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(ncalls):
+                    layers[i % R](xd, out=yd, stream=stream)
+        return g
+
+    full, rem = divmod(args.steps, chunk)
+    g_chunk = capture(chunk) if full else None
+    g_rem = capture(rem) if rem else None
+    for _ in range(2):
+        if g_chunk:
+            g_chunk.replay()
+    stream.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(full):
+        g_chunk.replay()
+    if g_rem:
+        g_rem.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    assert layers[0].get_error() == 0
+
+    # End to end through the host-buffer entry point (pinned host memory).
+    e2e_steps = min(args.steps, args.e2e_steps)
+    xh = torch.from_numpy(x).pin_memory().numpy()
+    yh = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory().numpy()
+    for i in range(min(R, 50)):
+        layers[i % R].forward_host(xh, yh, stream=stream)
+    if pg:
+        pg.barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        layers[i % R].forward_host(xh, yh, stream=stream)
+    e2e_s = time.perf_counter() - t0
+    if pg:
+        t = torch.tensor([e2e_s], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    peaks, peak_kind = measured_peaks()
+    s_per_step = ms / 1e3 / args.steps
+    tokens_per_s = ws * w.M / s_per_step
+    algo_bytes = w.algorithmic_bytes()
+    achieved = algo_bytes / s_per_step / 1e9
+    line = {
+        "metric": METRIC,
+        "value": tokens_per_s,
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64: Bernoulli(0.5) bits, U[0.005,0.03] fp16 scales, +-1 signs, N(0,1) x)",
+        "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "perm": w.perm,
+                   "weight_copies": R, "weight_set_bytes": R * wbytes,
+                   "l2": f"inputs larger than L2: {R} distinct weight copies ({R * wbytes / 1e6:.0f} MB) cycled",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "weight_gbs": w.weight_bytes() / s_per_step / 1e9,
+        "hbm_frac_of_8tbs": achieved / 8000.0,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "peak_kind": peak_kind,
+                     "kernel": "decode_kernel", "bytes_per_launch": algo_bytes,
+                     "traffic": traffic_record("decode_kernel", w.name)},
+        "gpu_launches": args.steps * (1 if w.M < 64 else 2),
+        "clocks": clocks,
+        "e2e": {"value": ws * w.M * e2e_steps / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": 4 * w.M * w.K, "d2h_bytes_per_step": 4 * w.M * w.N,
+                "steps": e2e_steps, "api": "bitlin_forward_host"},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inputs, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    for layer in layers:
+        layer.close()
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,333 @@
+// C-ABI of libbitlin: handle lifetime, argument checks, scratch management
+// and dispatch between the decode GEMV and the tensor-core path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "bitlin_internal.cuh"
+
+using namespace bitlin_impl;
+
+namespace {
+
+constexpr long long kDefaultWaitBudgetNs = 2000000000LL;  // 2 s per bounded wait
+
+bitlin_status from_cuda(bitlin_t h, cudaError_t e)
+{
+    if (e == cudaSuccess) return BITLIN_OK;
+    if (h) h->last_cuda_error = (int)e;
+    return e == cudaErrorMemoryAllocation ? BITLIN_ENOMEM : BITLIN_ECUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <typename T>
+void free_dev(T*& p)
+{
+    if (p) cudaFree(p);
+    p = nullptr;
+}
+
+void release(bitlin_t h)
+{
+    free_dev(h->dbits);
+    free_dev(h->dscales);
+    free_dev(h->pbits);
+    free_dev(h->pscales);
+    free_dev(h->signs);
+    free_dev(h->partials);
+    free_dev(h->counters);
+    free_dev(h->xt);
+    free_dev(h->dev_error);
+    free_dev(h->hx);
+    free_dev(h->hy);
+    if (h->h_err) cudaFreeHost(h->h_err);
+    h->h_err = nullptr;
+}
+
+cudaError_t ensure_partials(bitlin_t h, int M)
+{
+    if (h->partials && h->partials_M >= M) return cudaSuccess;
+    free_dev(h->partials);
+    h->partials_M = 0;
+    const size_t n = (size_t)h->S * M * h->T * kTileRows;
+    cudaError_t e = cudaMalloc(&h->partials, n * sizeof(float));
+    if (e == cudaSuccess) h->partials_M = M;
+    return e;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// Rotated-activation buffer (bf16 [M][K]) and its TMA descriptor.
+bitlin_status ensure_xt(bitlin_t h, int M)
+{
+    if (!h->xt || h->xt_M < M) {
+        free_dev(h->xt);
+        h->xt_M = 0;
+        h->tmap_M = 0;
+        cudaError_t e = cudaMalloc(&h->xt, (size_t)M * h->K * 2);
+        if (e != cudaSuccess) return from_cuda(h, e);
+        h->xt_M = M;
+    }
+    if (h->tmap_M != M) {
+        PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+        if (!enc) return from_cuda(h, cudaErrorNotSupported);
+        cuuint64_t dims[2] = {(cuuint64_t)h->K, (cuuint64_t)M};
+        cuuint64_t strides[1] = {(cuuint64_t)h->K * 2};
+        cuuint32_t box[2] = {64, (cuuint32_t)kPrefillTokens};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult r = enc(reinterpret_cast<CUtensorMap*>(h->tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                         h->xt, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return from_cuda(h, cudaErrorInvalidValue);
+        h->tmap_M = M;
+    }
+    return BITLIN_OK;
+}
+
+bitlin_status run_decode(bitlin_t h, const float* x, int M, float* y, cudaStream_t s)
+{
+    cudaError_t e = ensure_partials(h, M);
+    if (e != cudaSuccess) return from_cuda(h, e);
+    DecodeParams p;
+    p.bits = h->dbits;
+    p.scales = h->dscales;
+    p.signs = h->signs;
+    p.x = x;
+    p.y = y;
+    p.partials = h->partials;
+    p.counters = h->counters;
+    p.M = M;
+    p.N = h->N;
+    p.K = h->K;
+    p.S = h->S;
+    p.T = h->T;
+    p.perm = h->perm;
+    return from_cuda(h, bitlin_launch_decode(p, h->num_sms, s));
+}
+
+bitlin_status run_prefill(bitlin_t h, const float* x, int M, float* y, cudaStream_t s)
+{
+    bitlin_status st = ensure_xt(h, M);
+    if (st != BITLIN_OK) return st;
+    cudaError_t e = bitlin_launch_rotate_bf16(x, h->signs, M, h->K, h->perm, h->xt, s);
+    if (e != cudaSuccess) return from_cuda(h, e);
+    PrefillParams p;
+    p.bits = h->pbits;
+    p.scales = h->pscales;
+    p.y = y;
+    p.dev_error = h->dev_error;
+    p.M = M;
+    p.N = h->N;
+    p.K = h->K;
+    p.wait_budget_ns = h->wait_budget_ns;
+    e = bitlin_launch_prefill(p, h->tmap, h->stall_test, s);
+    return from_cuda(h, e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int bitlin_version(void) { return 100; }
+
+const char* bitlin_status_string(bitlin_status s)
+{
+    switch (s) {
+    case BITLIN_OK: return "success";
+    case BITLIN_EINVAL: return "invalid argument";
+    case BITLIN_ENOMEM: return "out of memory";
+    case BITLIN_ECUDA: return "CUDA runtime error";
+    case BITLIN_ETIMEOUT: return "a bounded device wait timed out";
+    case BITLIN_EDEVICE: return "the current device is not an sm_103 GPU";
+    }
+    return "unknown status";
+}
+
+bitlin_status bitlin_create(bitlin_t* out, int N, int K, const uint32_t* packed_bits,
+                            const uint16_t* scales, const float* signs, int perm_flag)
+{
+    if (!out) return BITLIN_EINVAL;
+    *out = nullptr;
+    if (!packed_bits || !scales || !signs || N < 1 || K < 1024 || K % 1024 != 0) return BITLIN_EINVAL;
+    if (perm_flag != BITLIN_PERM_NONE && perm_flag != BITLIN_PERM_SSM_TILED_TO_GROUPED) return BITLIN_EINVAL;
+    if (perm_flag == BITLIN_PERM_SSM_TILED_TO_GROUPED && K != 6144) return BITLIN_EINVAL;
+    if (!aligned16(packed_bits) || !aligned16(scales) || !aligned16(signs)) return BITLIN_EINVAL;
+    if ((long long)N * (K / 32) > (1LL << 40)) return BITLIN_EINVAL;
+
+    int dev = 0, major = 0, minor = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BITLIN_EDEVICE;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3) return BITLIN_EDEVICE;
+
+    bitlin_t h = new (std::nothrow) bitlin();
+    if (!h) return BITLIN_ENOMEM;
+    h->device = dev;
+    h->num_sms = sms;
+    h->N = N;
+    h->K = K;
+    h->perm = perm_flag;
+    h->S = K / kSlice;
+    h->T = (N + kTileRows - 1) / kTileRows;
+    h->wait_budget_ns = kDefaultWaitBudgetNs;
+    if (const char* env = getenv("BITLIN_WAIT_BUDGET_NS")) {
+        long long v = atoll(env);
+        if (v > 0) h->wait_budget_ns = v;
+    }
+
+    const size_t units = (size_t)h->S * h->T;
+    const size_t words = (size_t)N * (K / 32);
+    const size_t groups = (size_t)N * (K / 128);
+    cudaStream_t st = nullptr;
+    int* bad = nullptr;
+    int bad_host = 0;
+    bitlin_status status = BITLIN_OK;
+    cudaError_t e = cudaSuccess;
+#define BITLIN_TRY(call)                      \
+    do {                                      \
+        e = (call);                           \
+        if (e != cudaSuccess) goto fail_cuda; \
+    } while (0)
+    BITLIN_TRY(cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking));
+    BITLIN_TRY(cudaMalloc(&h->dbits, units * 4 * 32 * sizeof(uint4)));
+    BITLIN_TRY(cudaMalloc(&h->dscales, units * 32 * sizeof(uint2)));
+    BITLIN_TRY(cudaMalloc(&h->pbits, words * sizeof(uint32_t)));
+    BITLIN_TRY(cudaMalloc(&h->pscales, groups * sizeof(uint16_t)));
+    BITLIN_TRY(cudaMalloc(&h->signs, (size_t)K * sizeof(float)));
+    BITLIN_TRY(cudaMalloc(&h->counters, (size_t)h->T * sizeof(unsigned)));
+    BITLIN_TRY(cudaMalloc(&h->dev_error, 2 * sizeof(int)));
+    BITLIN_TRY(cudaHostAlloc(&h->h_err, sizeof(int), cudaHostAllocDefault));
+    bad = h->dev_error + 1;
+    BITLIN_TRY(cudaMemsetAsync(h->counters, 0, (size_t)h->T * sizeof(unsigned), st));
+    BITLIN_TRY(cudaMemsetAsync(h->dev_error, 0, 2 * sizeof(int), st));
+    BITLIN_TRY(cudaMemcpyAsync(h->signs, signs, (size_t)K * sizeof(float), cudaMemcpyDeviceToDevice, st));
+    BITLIN_TRY(cudaMemcpyAsync(h->pscales, scales, groups * sizeof(uint16_t), cudaMemcpyDeviceToDevice, st));
+    BITLIN_TRY(bitlin_launch_check_signs(h->signs, K, bad, st));
+    BITLIN_TRY(bitlin_launch_repack_decode(packed_bits, scales, N, K, h->dbits, h->dscales, st));
+    BITLIN_TRY(bitlin_launch_repack_prefill(packed_bits, N, K, h->pbits, st));
+    BITLIN_TRY(cudaMemcpyAsync(&bad_host, bad, sizeof(int), cudaMemcpyDeviceToHost, st));
+    BITLIN_TRY(cudaStreamSynchronize(st));
+    cudaStreamDestroy(st);
+    st = nullptr;
+    if (bad_host != 0) {
+        status = BITLIN_EINVAL;
+        goto fail;
+    }
+    *out = h;
+    return BITLIN_OK;
+#undef BITLIN_TRY
+fail_cuda:
+    status = (e == cudaErrorMemoryAllocation) ? BITLIN_ENOMEM : BITLIN_ECUDA;
+fail:
+    if (st) {
+        cudaStreamSynchronize(st);
+        cudaStreamDestroy(st);
+    }
+    release(h);
+    delete h;
+    return status;
+}
+
+bitlin_status bitlin_set_path(bitlin_t h, int path)
+{
+    if (!h || path < BITLIN_PATH_AUTO || path > BITLIN_PATH_PREFILL) return BITLIN_EINVAL;
+    h->path = path;
+    return BITLIN_OK;
+}
+
+bitlin_status bitlin_set_wait_budget(bitlin_t h, long long ns)
+{
+    if (!h || ns <= 0) return BITLIN_EINVAL;
+    h->wait_budget_ns = ns;
+    return BITLIN_OK;
+}
+
+bitlin_status bitlin_test_stall(bitlin_t h, int on)
+{
+    if (!h) return BITLIN_EINVAL;
+    h->stall_test = on ? 1 : 0;
+    return BITLIN_OK;
+}
+
+bitlin_status bitlin_forward(bitlin_t h, const float* x, int M, float* y, bitlin_stream_t stream)
+{
+    if (!h || !x || !y || M < 1) return BITLIN_EINVAL;
+    if (h->sticky != BITLIN_OK) return h->sticky;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int path = h->path;
+    if (path == BITLIN_PATH_AUTO) path = (M >= kPrefillMinM) ? BITLIN_PATH_PREFILL : BITLIN_PATH_DECODE;
+    return path == BITLIN_PATH_PREFILL ? run_prefill(h, x, M, y, s) : run_decode(h, x, M, y, s);
+}
+
+bitlin_status bitlin_forward_host(bitlin_t h, const float* x_host, int M, float* y_host,
+                                  bitlin_stream_t stream)
+{
+    if (!h || !x_host || !y_host || M < 1) return BITLIN_EINVAL;
+    if (h->sticky != BITLIN_OK) return h->sticky;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (!h->hx || h->h_M < M) {
+        free_dev(h->hx);
+        free_dev(h->hy);
+        h->h_M = 0;
+        e = cudaMalloc(&h->hx, (size_t)M * h->K * sizeof(float));
+        if (e == cudaSuccess) e = cudaMalloc(&h->hy, (size_t)M * h->N * sizeof(float));
+        if (e != cudaSuccess) return from_cuda(h, e);
+        h->h_M = M;
+    }
+    e = cudaMemcpyAsync(h->hx, x_host, (size_t)M * h->K * sizeof(float), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return from_cuda(h, e);
+    bitlin_status st = bitlin_forward(h, h->hx, M, h->hy, stream);
+    if (st != BITLIN_OK) return st;
+    e = cudaMemcpyAsync(y_host, h->hy, (size_t)M * h->N * sizeof(float), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->h_err, h->dev_error, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return from_cuda(h, e);
+    if (*h->h_err == kDevErrTimeout) h->sticky = BITLIN_ETIMEOUT;
+    return h->sticky;
+}
+
+bitlin_status bitlin_get_error(bitlin_t h)
+{
+    if (!h) return BITLIN_EINVAL;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return from_cuda(h, e);
+    int v = 0;
+    e = cudaMemcpy(&v, h->dev_error, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return from_cuda(h, e);
+    if (v == kDevErrTimeout) h->sticky = BITLIN_ETIMEOUT;
+    return h->sticky;
+}
+
+int bitlin_cuda_error(bitlin_t h) { return h ? h->last_cuda_error : 0; }
+
+bitlin_status bitlin_destroy(bitlin_t h)
+{
+    if (!h) return BITLIN_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    release(h);
+    delete h;
+    return e == cudaSuccess ? BITLIN_OK : BITLIN_ECUDA;
+}
+
+}  // extern "C"

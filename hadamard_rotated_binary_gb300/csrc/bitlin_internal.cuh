@@ -1,0 +1,99 @@
+// Internal declarations shared by the bitlin CUDA sources (not part of the C-ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bitlin.h"
+
+namespace bitlin_impl {
+
+// ---- decode layout -------------------------------------------------------
+// The decode GEMV works on units of (32 rows) x (512 weights along K): a
+// "tile" of one "slice".  Each slice is half of a 1024-wide transform block.
+constexpr int kSlice = 512;           // weights along K per lookup table
+constexpr int kTileRows = 32;         // rows per tile (one row per lane)
+constexpr int kWordsPerSlice = 16;    // uint32 words of one row in one slice
+constexpr int kGroupsPerSlice = 4;    // 128-weight scale groups per slice
+constexpr int kDecodeThreads = 512;   // 16 warps per CTA
+constexpr int kDecodeWarps = kDecodeThreads / 32;
+constexpr int kLutBytes = 65536;      // 64 octet tables x 256 entries x f32
+
+// ---- prefill layout ------------------------------------------------------
+constexpr int kPrefillRows = 128;     // weight rows per CTA (UMMA M)
+constexpr int kPrefillTokens = 128;   // tokens per CTA (UMMA N)
+constexpr int kPrefillStages = 3;
+constexpr int kPrefillMinM = 64;      // auto path switch
+
+// Device-side error word values (bitlin_t::dev_error).
+constexpr int kDevErrTimeout = 1;
+
+struct DecodeParams {
+    const uint4* bits;      // [S][T][4][32] uint4 (repacked, see repack.cu)
+    const uint2* scales;    // [S][T][32] uint2 (4 x fp16 per lane)
+    const float* signs;     // [K]
+    const float* x;         // [M][K]
+    float* y;               // [M][N]
+    float* partials;        // [S][M][T*32]
+    unsigned* counters;     // [T], zero between calls
+    int M, N, K, S, T, perm;
+};
+
+struct PrefillParams {
+    const uint32_t* bits;   // [N][K/32], prefill bit order (see repack.cu)
+    const uint16_t* scales; // [N][K/128]
+    float* y;               // [M][N]
+    int* dev_error;
+    int M, N, K;
+    long long wait_budget_ns;
+};
+
+}  // namespace bitlin_impl
+
+struct bitlin {
+    int device = 0;
+    int num_sms = 0;
+    int N = 0, K = 0, perm = 0;
+    int S = 0, T = 0;
+    int path = BITLIN_PATH_AUTO;
+    int last_cuda_error = 0;
+    bitlin_status sticky = BITLIN_OK;
+
+    // decode copy of the weights
+    uint4* dbits = nullptr;
+    uint2* dscales = nullptr;
+    // prefill copy of the weights
+    uint32_t* pbits = nullptr;
+    uint16_t* pscales = nullptr;
+    float* signs = nullptr;
+
+    // scratch
+    float* partials = nullptr;
+    int partials_M = 0;
+    unsigned* counters = nullptr;
+    void* xt = nullptr;        // bf16 [M][K] rotated activations for the prefill path
+    int xt_M = 0;
+    alignas(64) unsigned char tmap[128];  // TMA descriptor of xt (a CUtensorMap)
+    int tmap_M = 0;
+    int* dev_error = nullptr;  // device error word [0]; [1] is create's sign check
+    int* h_err = nullptr;      // pinned copy of the error word
+    long long wait_budget_ns = 0;
+    int stall_test = 0;
+
+    // host-buffer entry point staging
+    float* hx = nullptr;
+    float* hy = nullptr;
+    int h_M = 0;
+};
+
+// Launchers (return a cudaError_t).
+cudaError_t bitlin_launch_repack_decode(const uint32_t* bits, const uint16_t* scales, int N, int K,
+                                        uint4* dbits, uint2* dscales, cudaStream_t s);
+cudaError_t bitlin_launch_repack_prefill(const uint32_t* bits, int N, int K, uint32_t* pbits,
+                                         cudaStream_t s);
+cudaError_t bitlin_launch_check_signs(const float* signs, int K, int* bad, cudaStream_t s);
+cudaError_t bitlin_launch_decode(const bitlin_impl::DecodeParams& p, int num_sms, cudaStream_t s);
+cudaError_t bitlin_launch_rotate_bf16(const float* x, const float* signs, int M, int K, int perm,
+                                      void* xt, cudaStream_t s);
+cudaError_t bitlin_launch_prefill(const bitlin_impl::PrefillParams& p, const void* tmap, int stall_test,
+                                  cudaStream_t s);

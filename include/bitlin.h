@@ -1,0 +1,157 @@
+/*
+ * bitlin - Hadamard-folded 1-bit weight matrix-vector (and matrix-matrix)
+ * product for NVIDIA GB300 (sm_103a).
+ *
+ * What it computes, for every token row m of x[M][K]:
+ *
+ *   1. if the handle was created with BITLIN_PERM_SSM_TILED_TO_GROUPED, the
+ *      ssm_out head permutation tiled [hd=128, nk=16, rep=3] -> grouped
+ *      [hd, rep, nk]: xp[d + 128*(r + 3*k)] = x[d + 128*(k + 16*r)];
+ *   2. xs = xp * signs (elementwise, signs[i] in {+1, -1});
+ *   3. xt = blockwise normalized Walsh-Hadamard transform of xs in blocks of
+ *      1024 (natural Sylvester order, H[i][j] = (-1)^popcount(i & j)),
+ *      scaled by 1/32;
+ *   4. y[m][n] = sum over groups g of 128 along K of
+ *          scale[n][g] * sum_{k in g} (bit(n, k) ? +1 : -1) * xt[k],
+ *      where bit(n, k) = (packed_bits[n][k >> 5] >> (k & 31)) & 1.
+ *
+ * Sources: steps 1-3 and their order are the activation side of the Hadamard
+ * fold in the Pulse engine's "ARCHITECTURE-SPEC" page (section on the
+ * Hadamard fold: optional tiled->grouped permutation, x = x * signs,
+ * normalized Sylvester-Walsh transform, block 1024, scale 1/32, then
+ * y = W @ x; and its ssm_out permutation paragraph).  Step 4 is the one-bit
+ * Q1G128 format of the "Inside the One-Bit Engine" page (first station: one
+ * bit per weight, 1 -> +1, 0 -> -1, one shared scale per 128 weights, group
+ * sum then one multiply by the scale; station on the embedding row: bit k is
+ * bit k&31 of word k>>5, scale index k>>7, IEEE binary16 scales).
+ *
+ * Paths: M < 64 runs the decode GEMV (f32 throughout; expected max relative
+ * L2 error per token row <= 1e-5 against an exact evaluation).  M >= 64 runs
+ * the tensor-core path: xt is rounded to bf16, the bits become +-1 bf16
+ * operands of tcgen05 MMAs with f32 accumulation, and each group's partial
+ * product is multiplied by its scale in f32 (expected error <= 1e-2).
+ *
+ * Errors: every function returns a bitlin_status and never aborts or prints.
+ * Threads: a handle may be used from one host thread / one stream at a time.
+ */
+#ifndef BITLIN_H
+#define BITLIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque handle owning a repacked device copy of one folded 1-bit matrix. */
+typedef struct bitlin* bitlin_t;
+
+/* A cudaStream_t (the runtime's stream type is this pointer type). */
+typedef struct CUstream_st* bitlin_stream_t;
+
+typedef enum {
+    BITLIN_OK = 0,
+    BITLIN_EINVAL = 1,   /* a NULL pointer, a size or flag out of range, a sign that is not +-1 */
+    BITLIN_ENOMEM = 2,   /* a device or host allocation failed */
+    BITLIN_ECUDA = 3,    /* a CUDA runtime call or kernel launch failed (see bitlin_cuda_error) */
+    BITLIN_ETIMEOUT = 4, /* a bounded wait inside a kernel gave up; the output is not valid */
+    BITLIN_EDEVICE = 5   /* the current device is not an sm_103 GPU */
+} bitlin_status;
+
+#define BITLIN_PERM_NONE 0
+/* ssm_out: tiled [hd=128, nk=16, rep=3] -> grouped [hd, rep, nk]; requires K == 6144.
+ * (Pulse "ARCHITECTURE-SPEC", ssm_out permutation paragraph.) */
+#define BITLIN_PERM_SSM_TILED_TO_GROUPED 1
+
+#define BITLIN_PATH_AUTO 0    /* M < 64 -> decode, M >= 64 -> tensor-core prefill */
+#define BITLIN_PATH_DECODE 1  /* force the f32 decode GEMV for every M */
+#define BITLIN_PATH_PREFILL 2 /* force the tcgen05 bf16 path for every M */
+
+/*
+ * Create a handle for one N x K folded 1-bit matrix on the current device.
+ *
+ *   packed_bits  device pointer, uint32 [N][K/32], row-major; bit k of row n is
+ *                bit (k & 31) of word k >> 5 (LSB first); 1 means +1, 0 means -1.
+ *   scales       device pointer, IEEE binary16 bit patterns [N][K/128], row-major.
+ *   signs        device pointer, float [K]; every entry exactly +1.0f or -1.0f.
+ *   perm_flag    BITLIN_PERM_NONE or BITLIN_PERM_SSM_TILED_TO_GROUPED.
+ *
+ * Requirements: N >= 1, K a positive multiple of 1024, all three pointers
+ * 16-byte aligned device memory.  The call copies and repacks its inputs into
+ * memory the handle owns and synchronizes before returning, so the caller may
+ * free or reuse the three arrays afterwards.
+ * Errors: BITLIN_EINVAL (NULL out/pointers, N < 1, K % 1024 != 0, unknown
+ * perm_flag, perm with K != 6144, a sign other than +-1), BITLIN_ENOMEM,
+ * BITLIN_ECUDA, BITLIN_EDEVICE.  On error *out is set to NULL.
+ */
+bitlin_status bitlin_create(bitlin_t* out, int N, int K, const uint32_t* packed_bits,
+                            const uint16_t* scales, const float* signs, int perm_flag);
+
+/*
+ * y[M][N] = the folded product of x[M][K] (see the top of this file).
+ *
+ *   x       device pointer, float [M][K], row-major, read only.
+ *   y       device pointer, float [M][N], row-major, fully overwritten; must not overlap x.
+ *   stream  CUDA stream the work is queued on (NULL = legacy default stream).
+ *
+ * Asynchronous: no host synchronization.  The first call with a new largest M
+ * (and the first call of the tensor-core path) allocates scratch memory the
+ * handle keeps; later calls with M at most that size allocate nothing, so they
+ * may be captured in a CUDA graph.  Decode launches use programmatic
+ * dependent launch: the kernel starts fetching weights while the previous
+ * kernel on the stream finishes, and reads x only after it has completed.
+ * Errors: BITLIN_EINVAL (NULL handle/x/y, M < 1), BITLIN_ENOMEM, BITLIN_ECUDA,
+ * and the sticky BITLIN_ETIMEOUT of an earlier call (see bitlin_get_error).
+ */
+bitlin_status bitlin_forward(bitlin_t h, const float* x, int M, float* y, bitlin_stream_t stream);
+
+/*
+ * The same product with x and y in HOST memory: copies x to the device, runs
+ * bitlin_forward on `stream`, copies y back and synchronizes the stream.
+ * Pinned host buffers give the fastest copies; pageable memory also works.
+ * Errors: as bitlin_forward, plus BITLIN_ETIMEOUT from this call's kernels.
+ */
+bitlin_status bitlin_forward_host(bitlin_t h, const float* x_host, int M, float* y_host,
+                                  bitlin_stream_t stream);
+
+/* Select the path used for later calls (BITLIN_PATH_*).  EINVAL on an unknown value. */
+bitlin_status bitlin_set_path(bitlin_t h, int path);
+
+/* Longest time, in nanoseconds, that any one wait inside the tensor-core
+ * kernel may take before the kernel gives up and records BITLIN_ETIMEOUT
+ * (default 2e9, or the BITLIN_WAIT_BUDGET_NS environment variable at create).
+ * EINVAL for ns <= 0. */
+bitlin_status bitlin_set_wait_budget(bitlin_t h, long long ns);
+
+/* Testing aid for the failure path: when on != 0, later tensor-core calls
+ * make their epilogue wait on a barrier that nothing ever arrives at, so the
+ * bounded wait runs out, the kernel drains and frees its resources, and
+ * bitlin_get_error / bitlin_forward_host report BITLIN_ETIMEOUT.  No fault,
+ * trap or hang is involved.  The timeout is sticky on the handle. */
+bitlin_status bitlin_test_stall(bitlin_t h, int on);
+
+/* Release everything the handle owns.  NULL is accepted.  Synchronizes the device. */
+bitlin_status bitlin_destroy(bitlin_t h);
+
+/*
+ * Wait for the handle's queued work and report a device-side failure
+ * recorded by its kernels (BITLIN_ETIMEOUT when a bounded wait gave up), or
+ * BITLIN_ECUDA if synchronizing failed.  The error stays set (sticky).
+ */
+bitlin_status bitlin_get_error(bitlin_t h);
+
+/* The cudaError_t value behind the last BITLIN_ECUDA of this handle (0 if none). */
+int bitlin_cuda_error(bitlin_t h);
+
+/* A static, human-readable description of a status value. */
+const char* bitlin_status_string(bitlin_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int bitlin_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITLIN_H */

@@ -1,0 +1,260 @@
+"""GPU parity of the CUDA path (through the C-ABI) against the CPU oracle.
+
+Every case draws its inputs from the seeded generator, runs the library on
+cuda:0, and compares with the oracle's f64 evaluation of the same inputs:
+max relative L2 error per token row <= 1e-5 on the decode path and <= 1e-2
+on the tensor-core path.  Full-size cases compare every output where the
+oracle finishes in seconds, else a seeded sample of rows (always including
+the first and last).
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+DECODE_TOL = 1e-5
+PREFILL_TOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def hrb():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from hadamard_rotated_binary_gb300 import build as hbuild
+
+    hbuild.build()
+    oracle.build()
+    import hadamard_rotated_binary_gb300 as m
+
+    return m
+
+
+def make_layer(hrb, bits, scales, signs, perm):
+    tb = torch.from_numpy(np.ascontiguousarray(bits).view(np.int32)).cuda()
+    ts = torch.from_numpy(np.ascontiguousarray(scales).view(np.int16)).cuda()
+    tg = torch.from_numpy(np.ascontiguousarray(signs)).cuda()
+    return hrb.BitLinear(tb, ts, tg, perm)
+
+
+def run(layer, x, path=None):
+    if path is not None:
+        layer.set_path(path)
+    y = layer(torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    assert layer.get_error() == 0
+    return y.cpu().numpy().astype(np.float64)
+
+
+def max_rel_l2(y, ref):
+    num = np.linalg.norm(y - ref, axis=1)
+    den = np.linalg.norm(ref, axis=1)
+    return float((num / den).max())
+
+
+def inputs(name, M=None):
+    w = synth.workload(name, M)
+    return (w,) + synth.make_inputs(w)
+
+
+# ------------------------------------------------------------------ decode
+
+def test_tiny_probe(hrb):
+    w, bits, scales, signs, x = inputs("tiny")
+    y = run(make_layer(hrb, bits, scales, signs, w.perm), x)
+    ref = oracle.forward(bits, scales, signs, w.perm, x)
+    assert max_rel_l2(y, ref) <= DECODE_TOL
+    # known-answer probe of 256 rows: no output off by more than 0.5
+    assert int((np.abs(y - ref) > 0.5).sum()) == 0
+    golden = np.loadtxt(os.path.join(os.path.dirname(__file__), "golden", "tiny_oracle.txt"))
+    assert max_rel_l2(y, golden[None, :]) <= DECODE_TOL
+
+
+@pytest.mark.parametrize("name", ["ffn_gate", "ffn_down", "ssm_out", "attn_output"])
+def test_decode_full_size_every_output(hrb, name):
+    w, bits, scales, signs, x = inputs(name)
+    y = run(make_layer(hrb, bits, scales, signs, w.perm), x)
+    ref = oracle.forward(bits, scales, signs, w.perm, x)
+    assert max_rel_l2(y, ref) <= DECODE_TOL
+
+
+def test_ssm_out_permutation_matters(hrb):
+    """The same ssm_out weights without the permutation must not match (Pulse spec:
+    skipping the permutation gives an unrelated answer)."""
+    w, bits, scales, signs, x = inputs("ssm_out")
+    y = run(make_layer(hrb, bits, scales, signs, 0), x)
+    ref = oracle.forward(bits, scales, signs, 1, x)
+    assert max_rel_l2(y, ref) > 0.5
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_gate_up_decode_sweep(hrb, M):
+    w, bits, scales, signs, x = inputs("gate_up", M)
+    y = run(make_layer(hrb, bits, scales, signs, w.perm), x)
+    rows = None if M == 1 else synth.sample_rows(w.seed, w.N, 1536)
+    ref = oracle.forward(bits, scales, signs, w.perm, x, rows)
+    got = y if rows is None else y[:, rows]
+    assert max_rel_l2(got, ref) <= DECODE_TOL
+
+
+def test_gate_up_m64_both_paths(hrb):
+    w, bits, scales, signs, x = inputs("gate_up", 64)
+    layer = make_layer(hrb, bits, scales, signs, w.perm)
+    rows = synth.sample_rows(w.seed, w.N, 1024)
+    ref = oracle.forward(bits, scales, signs, w.perm, x, rows)
+    y_auto = run(layer, x)  # M = 64 selects the tensor-core path
+    assert max_rel_l2(y_auto[:, rows], ref) <= PREFILL_TOL
+    y_dec = run(layer, x, path=hrb.PATH_DECODE)
+    assert max_rel_l2(y_dec[:, rows], ref) <= DECODE_TOL
+
+
+# ------------------------------------------------------------------ prefill
+
+def test_prefill_full_size_sampled_rows(hrb):
+    w, bits, scales, signs, x = inputs("prefill")
+    y = run(make_layer(hrb, bits, scales, signs, w.perm), x)
+    rows = synth.sample_rows(w.seed, w.N, 160)
+    ref = oracle.forward(bits, scales, signs, w.perm, x, rows)
+    assert max_rel_l2(y[:, rows], ref) <= PREFILL_TOL
+    # against the oracle with bf16-rounded activations the error is only the
+    # f32 accumulation order
+    ref16 = oracle.forward(bits, scales, signs, w.perm, x, rows, round_bf16=True)
+    assert max_rel_l2(y[:, rows], ref16) <= 1e-4
+    assert np.all(np.isfinite(y))
+
+
+@pytest.mark.parametrize("N,K,M,perm", [(300, 2048, 65, 0), (129, 1024, 130, 0), (256, 6144, 128, 1),
+                                        (1000, 3072, 200, 0)])
+def test_prefill_ragged(hrb, N, K, M, perm):
+    seed = 7 + N + K + M
+    bits = synth.random_bits(seed, N, K)
+    scales = synth.random_scales(seed, N, K, 0.005, 0.03)
+    signs = synth.random_signs(seed, K)
+    x = synth.random_x(seed, M, K)
+    y = run(make_layer(hrb, bits, scales, signs, perm), x)
+    ref = oracle.forward(bits, scales, signs, perm, x)
+    assert max_rel_l2(y, ref) <= PREFILL_TOL
+    ref16 = oracle.forward(bits, scales, signs, perm, x, round_bf16=True)
+    assert max_rel_l2(y, ref16) <= 1e-4
+
+
+# ------------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("N,K,M", [(1, 1024, 1), (100, 1024, 1), (31, 2048, 3), (1000, 3072, 5),
+                                   (4097, 1024, 2), (33, 17408, 1)])
+def test_decode_ragged(hrb, N, K, M):
+    seed = 11 + N + K + M
+    bits = synth.random_bits(seed, N, K)
+    scales = synth.random_scales(seed, N, K, 0.005, 0.03)
+    signs = synth.random_signs(seed, K)
+    x = synth.random_x(seed, M, K)
+    y = run(make_layer(hrb, bits, scales, signs, 0), x)
+    ref = oracle.forward(bits, scales, signs, 0, x)
+    assert max_rel_l2(y, ref) <= DECODE_TOL
+
+
+def test_prefill_path_forced_at_one_token(hrb):
+    w, bits, scales, signs, x = inputs("tiny")
+    y = run(make_layer(hrb, bits, scales, signs, 0), x, path=hrb.PATH_PREFILL)
+    ref = oracle.forward(bits, scales, signs, 0, x)
+    assert max_rel_l2(y, ref) <= PREFILL_TOL
+
+
+def test_degenerate_all_ones_and_zero_input(hrb):
+    N, K = 64, 2048
+    scales = synth.random_scales(3, N, K, 0.005, 0.03)
+    signs = synth.random_signs(3, K)
+    x = synth.random_x(3, 2, K)
+    ones = np.full((N, K // 32), 0xFFFFFFFF, dtype=np.uint32)
+    layer = make_layer(hrb, ones, scales, signs, 0)
+    y = run(layer, x)
+    ref = oracle.forward(ones, scales, signs, 0, x)
+    assert max_rel_l2(y, ref) <= DECODE_TOL
+    z = run(layer, np.zeros_like(x))
+    assert np.all(z == 0.0)
+
+
+def test_repeat_calls_are_bitwise_identical(hrb):
+    w, bits, scales, signs, x = inputs("ffn_down")
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    xd = torch.from_numpy(x).cuda()
+    a = layer(xd).clone()
+    b = layer(xd).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_alternating_token_counts_reuse_scratch(hrb):
+    w, bits, scales, signs, x = inputs("ffn_gate", 8)
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    rows = synth.sample_rows(w.seed, w.N, 512)
+    ref = oracle.forward(bits, scales, signs, 0, x, rows)
+    for m in (8, 1, 3, 8):
+        y = run(layer, x[:m].copy())
+        assert max_rel_l2(y[:, rows], ref[:m]) <= DECODE_TOL
+
+
+def test_cuda_graph_replay_matches(hrb):
+    w, bits, scales, signs, x = inputs("ffn_gate")
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    xd = torch.from_numpy(x).cuda()
+    yd = torch.empty((1, w.N), device="cuda")
+    layer(xd, out=yd)  # warm-up allocates the scratch
+    torch.cuda.synchronize()
+    eager = yd.clone()
+    yd.zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(3):
+                layer(xd, out=yd, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(yd, eager)
+
+
+def test_forward_host_buffers(hrb):
+    w, bits, scales, signs, x = inputs("ssm_out")
+    layer = make_layer(hrb, bits, scales, signs, w.perm)
+    y = np.empty((1, w.N), dtype=np.float32)
+    layer.forward_host(x, y)
+    ref = oracle.forward(bits, scales, signs, w.perm, x)
+    assert max_rel_l2(y.astype(np.float64), ref) <= DECODE_TOL
+
+
+# ------------------------------------------------------------------ errors
+
+def test_signs_must_be_plus_minus_one(hrb):
+    w, bits, scales, signs, x = inputs("tiny")
+    bad = signs.copy()
+    bad[5] = 0.5
+    with pytest.raises(hrb.BitlinError) as e:
+        make_layer(hrb, bits, scales, bad, 0)
+    assert e.value.status == hrb.BITLIN_EINVAL
+
+
+def test_bounded_wait_times_out_without_hanging(hrb):
+    """A barrier nobody arrives at: the kernel gives up after its budget,
+    releases its resources and reports a timeout; the context stays usable."""
+    w, bits, scales, signs, x = inputs("tiny")
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    layer.set_path(hrb.PATH_PREFILL)
+    layer.set_wait_budget(200_000_000)  # 0.2 s
+    layer.test_stall(True)
+    layer(torch.from_numpy(x).cuda())
+    assert layer.get_error() == hrb.BITLIN_ETIMEOUT
+    with pytest.raises(hrb.BitlinError):
+        layer(torch.from_numpy(x).cuda())
+    layer.close()
+    fresh = make_layer(hrb, bits, scales, signs, 0)
+    y = run(fresh, x)
+    assert max_rel_l2(y, oracle.forward(bits, scales, signs, 0, x)) <= DECODE_TOL
