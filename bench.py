@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--ref-seconds", type=float, default=90.0)
     ap.add_argument("--e2e-steps", type=int, default=20000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--copies", type=int, default=0,
+                    help="distinct weight copies to cycle (default: enough for 4x the L2 size)")
     return ap.parse_args()
 
 
@@ -249,7 +251,7 @@ def main():
     tg = torch.from_numpy(signs).to(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     wbytes = w.weight_bytes()
-    R = max(2, -(-4 * l2 // wbytes))
+    R = args.copies if args.copies else max(2, -(-4 * l2 // wbytes))
     layers = [hrb.BitLinear(tb, ts, tg, w.perm) for _ in range(R)]
     del tb, ts, tg
     xd = torch.from_numpy(x).to(dev)
@@ -274,9 +276,10 @@ def main():
     full, rem = divmod(args.steps, chunk)
     g_chunk = capture(chunk) if full else None
     g_rem = capture(rem) if rem else None
-    for _ in range(2):
-        if g_chunk:
-            g_chunk.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            if g_chunk:
+                g_chunk.replay()
     stream.synchronize()
 
     sampler = ClockSampler(local)
@@ -287,12 +290,13 @@ def main():
     torch.cuda.synchronize(dev)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(full):
-        g_chunk.replay()
-    if g_rem:
-        g_rem.replay()
-    ev1.record(stream)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        ev0.record(stream)
+        for _ in range(full):
+            g_chunk.replay()
+        if g_rem:
+            g_rem.replay()
+        ev1.record(stream)
     torch.cuda.synchronize(dev)
     if pg:
         pg.barrier()

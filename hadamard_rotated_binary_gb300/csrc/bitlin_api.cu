@@ -214,11 +214,11 @@ bitlin_status bitlin_create(bitlin_t* out, int N, int K, const uint32_t* packed_
     BITLIN_TRY(cudaMalloc(&h->pbits, words * sizeof(uint32_t)));
     BITLIN_TRY(cudaMalloc(&h->pscales, groups * sizeof(uint16_t)));
     BITLIN_TRY(cudaMalloc(&h->signs, (size_t)K * sizeof(float)));
-    BITLIN_TRY(cudaMalloc(&h->counters, (size_t)h->T * sizeof(unsigned)));
+    BITLIN_TRY(cudaMalloc(&h->counters, (size_t)h->T * kTicketStride * sizeof(unsigned)));
     BITLIN_TRY(cudaMalloc(&h->dev_error, 2 * sizeof(int)));
     BITLIN_TRY(cudaHostAlloc(&h->h_err, sizeof(int), cudaHostAllocDefault));
     bad = h->dev_error + 1;
-    BITLIN_TRY(cudaMemsetAsync(h->counters, 0, (size_t)h->T * sizeof(unsigned), st));
+    BITLIN_TRY(cudaMemsetAsync(h->counters, 0, (size_t)h->T * kTicketStride * sizeof(unsigned), st));
     BITLIN_TRY(cudaMemsetAsync(h->dev_error, 0, 2 * sizeof(int), st));
     BITLIN_TRY(cudaMemcpyAsync(h->signs, signs, (size_t)K * sizeof(float), cudaMemcpyDeviceToDevice, st));
     BITLIN_TRY(cudaMemcpyAsync(h->pscales, scales, groups * sizeof(uint16_t), cudaMemcpyDeviceToDevice, st));

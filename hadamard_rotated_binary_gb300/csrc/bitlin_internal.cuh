@@ -15,9 +15,13 @@ constexpr int kSlice = 512;           // weights along K per lookup table
 constexpr int kTileRows = 32;         // rows per tile (one row per lane)
 constexpr int kWordsPerSlice = 16;    // uint32 words of one row in one slice
 constexpr int kGroupsPerSlice = 4;    // 128-weight scale groups per slice
-constexpr int kDecodeThreads = 512;   // 16 warps per CTA
+#ifndef BITLIN_DECODE_THREADS
+#define BITLIN_DECODE_THREADS 256
+#endif
+constexpr int kDecodeThreads = BITLIN_DECODE_THREADS;  // 8 warps per CTA: two CTAs fit on an SM
 constexpr int kDecodeWarps = kDecodeThreads / 32;
 constexpr int kLutBytes = 65536;      // 64 octet tables x 256 entries x f32
+constexpr int kTicketStride = 32;     // one split-K ticket per 128-byte line
 
 // ---- prefill layout ------------------------------------------------------
 constexpr int kPrefillRows = 128;     // weight rows per CTA (UMMA M)
@@ -35,8 +39,9 @@ struct DecodeParams {
     const float* x;         // [M][K]
     float* y;               // [M][N]
     float* partials;        // [S][M][T*32]
-    unsigned* counters;     // [T], zero between calls
+    unsigned* counters;     // [T * kTicketStride], zero between calls
     int M, N, K, S, T, perm;
+    int ctas_per_slice;     // set by the launcher
 };
 
 struct PrefillParams {

@@ -8,7 +8,7 @@
 //
 // How (GB300 design):
 //  * Work unit = (slice s of 512 weights along K) x (tile t of 32 rows).  A CTA
-//    (16 warps, one per SM) takes a contiguous run of units, so it touches one
+//    (8 warps, one per SM) takes a contiguous run of units, so it touches one
 //    or two slices; split-K partial sums land in a scratch array and the last
 //    contributor of each tile (an atomic ticket per tile) adds the slices in
 //    fixed order s = 0..S-1 - deterministic results.
@@ -32,9 +32,12 @@
 //    register), one LDS and one FADD.  Every 4 words (one 128-group) the
 //    group sum is multiplied by its fp16 scale with one FFMA.
 //  * Weights stream straight from HBM into registers with 16-byte coalesced
-//    loads; each warp prefetches its next tile while it computes the current
-//    one, and the first tile is requested before the prologue so that DRAM
-//    latency overlaps the transform and the table build.
+//    loads through a ring of 4 tiles per warp: the first 4 tiles are requested
+//    before the prologue (so DRAM latency overlaps the transform and the table
+//    build) and each consumed tile is replaced by the warp's next one.
+//  * At most 128 registers and 70 KB of shared memory per CTA, so a second
+//    CTA fits on each SM: the next call's CTAs become resident while this
+//    call finishes and start streaming their weights.
 //  * Programmatic dependent launch: the kernel lets its successor launch at
 //    once and itself waits (griddepcontrol.wait) only before it reads x or
 //    writes any output; weight prefetch precedes the wait.
@@ -50,6 +53,8 @@ constexpr int kPad = 33;                               // transpose row stride (
 constexpr int kSmemTranspose = 16 * kPad * 4;           // 2112 B
 constexpr int kSmemSlice = (kSlice + kSlice / 32) * 4;  // 528 floats
 constexpr int kDecodeSmem = kLutBytes + kSmemTranspose + kSmemSlice;
+constexpr int kRowsPerWarp = 16 / kDecodeWarps;  // rows of the [16][32] transform view per warp
+static_assert(kDecodeWarps == 8 || kDecodeWarps == 16, "prologue mapping assumes 8 or 16 warps");
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents()
@@ -84,45 +89,73 @@ __device__ __forceinline__ int perm_source(int k)
     return d + 128 * (kk + 16 * r);
 }
 
-// Rotated activations of token m for slice s into xs (padded, 512 floats).
-__device__ __forceinline__ void build_slice(const DecodeParams& p, int m, int s, float* tbuf,
-                                            float* xs, int warp, int lane)
+// Rotated activations of token m for slice s, in two parts so that the
+// caller can issue other loads between them.  Thread (warp w, lane q) covers
+// rows p = w and p = w + 8 of the [16][32] view of the half block.
+// slice_load: the raw x and sign values (gather through the ssm_out
+// permutation when requested); no arithmetic, so nothing waits on them yet.
+__device__ __forceinline__ void slice_load(const DecodeParams& p, int m, int s, int warp, int lane,
+                                           float (&v)[4 * kRowsPerWarp])
 {
-    const int b = s >> 1, h = s & 1;
-    const int i = 32 * warp + lane;  // 0..511
-    const int k0 = b * 1024 + i, k1 = k0 + 512;
+    const int b = s >> 1;
     const float* xm = p.x + (size_t)m * p.K;
-    const int src0 = p.perm ? perm_source(k0) : k0;
-    const int src1 = p.perm ? perm_source(k1) : k1;
-    const float a = __ldg(xm + src0) * __ldg(p.signs + k0);
-    const float c = __ldg(xm + src1) * __ldg(p.signs + k1);
-    float v = h ? (a - c) : (a + c);
-    // 32-point butterflies across the lanes (natural Sylvester order).
 #pragma unroll
-    for (int st = 1; st < 32; st <<= 1) {
-        const float o = __shfl_xor_sync(0xffffffffu, v, st);
-        v = (lane & st) ? (o - v) : (v + o);
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        const int i = 32 * (warp + kDecodeWarps * r) + lane;  // 0..511
+        const int k0 = b * 1024 + i, k1 = k0 + 512;
+        const int src0 = p.perm ? perm_source(k0) : k0;
+        const int src1 = p.perm ? perm_source(k1) : k1;
+        v[4 * r + 0] = __ldg(xm + src0);
+        v[4 * r + 1] = __ldg(p.signs + k0);
+        v[4 * r + 2] = __ldg(xm + src1);
+        v[4 * r + 3] = __ldg(p.signs + k1);
     }
-    tbuf[warp * kPad + lane] = v;
+}
+
+// slice_transform: half h of the block's 1024-point transform is
+// H512(xs_lo + (-1)^h xs_hi) / 32 with H512 = H16 (x) H32; the result goes to xs
+// (padded, 512 floats).
+__device__ __forceinline__ void slice_transform(int s, const float (&v)[4 * kRowsPerWarp], float* tbuf, float* xs,
+                                                int warp, int lane)
+{
+    const int h = s & 1;
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        const float a = v[4 * r + 0] * v[4 * r + 1];
+        const float c = v[4 * r + 2] * v[4 * r + 3];
+        float z = h ? (a - c) : (a + c);
+        // 32-point butterflies across the lanes (natural Sylvester order).
+#pragma unroll
+        for (int st = 1; st < 32; st <<= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, z, st);
+            z = (lane & st) ? (o - z) : (z + o);
+        }
+        tbuf[(warp + kDecodeWarps * r) * kPad + lane] = z;
+    }
     __syncthreads();
-    // 16-point butterflies down the columns: warp w takes columns 2w, 2w+1.
-    const int col = 2 * warp + (lane >> 4), row = lane & 15;
-    float z = tbuf[row * kPad + col];
+    // 16-point butterflies down the columns: warp w takes 32 / warps columns,
+    // one per half-warp and round; lane & 15 is the row.
+    const int row = lane & 15;
 #pragma unroll
-    for (int st = 1; st < 16; st <<= 1) {
-        const float o = __shfl_xor_sync(0xffffffffu, z, st);
-        z = (row & st) ? (o - z) : (z + o);
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        const int col = 2 * kRowsPerWarp * warp + 2 * r + (lane >> 4);
+        float z = tbuf[row * kPad + col];
+#pragma unroll
+        for (int st = 1; st < 16; st <<= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, z, st);
+            z = (row & st) ? (o - z) : (z + o);
+        }
+        xs[xpad(row * 32 + col)] = z * 0.03125f;  // exact scaling by 1/32
     }
-    xs[xpad(row * 32 + col)] = z * 0.03125f;  // exact scaling by 1/32
     __syncthreads();
 }
 
-// Signed-sum tables for the slice: warp v writes entries b = 16v .. 16v+15 of
-// all 64 tables; lane L writes the two tables of bank L (its word w = L & 15,
-// byte parity L >> 4, byte pair jh = 0, 1).
+// Signed-sum tables for the slice: warp v writes entries b = 16*hn .. 16*hn+15
+// (high nibbles hn = v, v + warps, ...) of all 64 tables; lane L writes the
+// two tables of bank L (its word w = L & 15, byte parity L >> 4, byte pair jh).
 __device__ __forceinline__ void build_tables(const float* xs, unsigned char* lut, int warp, int lane)
 {
-    const int w = lane & 15, jlo = lane >> 4, hnib = warp;
+    const int w = lane & 15, jlo = lane >> 4;
 #pragma unroll
     for (int jh = 0; jh < 2; ++jh) {
         const int j = 2 * jh + jlo;
@@ -139,45 +172,70 @@ __device__ __forceinline__ void build_tables(const float* xs, unsigned char* lut
         p23[1] = x[2] - x[3];
         p23[2] = x[3] - x[2];
         p23[3] = x[2] + x[3];
-        const float a45 = ((hnib & 1) ? x[4] : -x[4]) + ((hnib & 2) ? x[5] : -x[5]);
-        const float a67 = ((hnib & 4) ? x[6] : -x[6]) + ((hnib & 8) ? x[7] : -x[7]);
-        const float hi = a45 + a67;
-        unsigned char* dst = lut + (size_t)(16 * hnib) * 256 + 128 * jh + 4 * lane;
 #pragma unroll
-        for (int l = 0; l < 16; ++l)
-            *reinterpret_cast<float*>(dst + l * 256) = (p01[l & 3] + p23[l >> 2]) + hi;
+        for (int hh = 0; hh < kRowsPerWarp; ++hh) {
+            const int hnib = warp + kDecodeWarps * hh;
+            const float a45 = ((hnib & 1) ? x[4] : -x[4]) + ((hnib & 2) ? x[5] : -x[5]);
+            const float a67 = ((hnib & 4) ? x[6] : -x[6]) + ((hnib & 8) ? x[7] : -x[7]);
+            const float hi = a45 + a67;
+            unsigned char* dst = lut + (size_t)(16 * hnib) * 256 + 128 * jh + 4 * lane;
+#pragma unroll
+            for (int l = 0; l < 16; ++l)
+                *reinterpret_cast<float*>(dst + l * 256) = (p01[l & 3] + p23[l >> 2]) + hi;
+        }
     }
 }
 
-// One tile's dot products for this lane's row: sum over the slice's 4 groups
-// of scale * (sum of 16 table lookups).
-__device__ __forceinline__ float tile_dot(const unsigned char* lut, const uint4 (&b)[4], uint2 sc,
-                                          uint32_t base_off)
+// Dot products of two tiles for this lane's two rows, interleaved so that the
+// two tiles' lookup chains are independent: per tile, the sum over the
+// slice's 4 groups of scale * (sum of 16 table lookups).
+__device__ __forceinline__ void tile_dot2(const unsigned char* lut, const uint4 (&b0)[4], uint2 sc0,
+                                          const uint4 (&b1)[4], uint2 sc1, uint32_t base_off,
+                                          float& out0, float& out1)
 {
-    const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sc.x));
-    const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sc.y));
-    const float scl[4] = {s01.x, s01.y, s23.x, s23.y};
-    float acc = 0.f;
+    float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-        const uint32_t wv[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
-        float g0 = 0.f, g1 = 0.f;
+        const uint32_t wa[4] = {b0[u].x, b0[u].y, b0[u].z, b0[u].w};
+        const uint32_t wb[4] = {b1[u].x, b1[u].y, b1[u].z, b1[u].w};
+        float ga0 = 0.f, ga1 = 0.f, gb0 = 0.f, gb1 = 0.f;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const uint32_t pos = 4u * u + c;
             const uint32_t off = base_off ^ ((4u * pos) * 0x101u);
-            const uint32_t wd = wv[c];
-            g0 += lut_at(lut, __byte_perm(wd, off, 0x7604));
-            g1 += lut_at(lut, __byte_perm(wd, off, 0x7615));
-            g0 += lut_at(lut + 128, __byte_perm(wd, off, 0x7624));
-            g1 += lut_at(lut + 128, __byte_perm(wd, off, 0x7635));
+            ga0 += lut_at(lut, __byte_perm(wa[c], off, 0x7604));
+            gb0 += lut_at(lut, __byte_perm(wb[c], off, 0x7604));
+            ga1 += lut_at(lut, __byte_perm(wa[c], off, 0x7615));
+            gb1 += lut_at(lut, __byte_perm(wb[c], off, 0x7615));
+            ga0 += lut_at(lut + 128, __byte_perm(wa[c], off, 0x7624));
+            gb0 += lut_at(lut + 128, __byte_perm(wb[c], off, 0x7624));
+            ga1 += lut_at(lut + 128, __byte_perm(wa[c], off, 0x7635));
+            gb1 += lut_at(lut + 128, __byte_perm(wb[c], off, 0x7635));
         }
-        acc = fmaf(g0 + g1, scl[u], acc);
+        const uint32_t ha = (u < 2 ? sc0.x : sc0.y) >> (16 * (u & 1));
+        const uint32_t hb = (u < 2 ? sc1.x : sc1.y) >> (16 * (u & 1));
+        acc0 = fmaf(ga0 + ga1, __half2float(__ushort_as_half((unsigned short)ha)), acc0);
+        acc1 = fmaf(gb0 + gb1, __half2float(__ushort_as_half((unsigned short)hb)), acc1);
     }
-    return acc;
+    out0 = acc0;
+    out1 = acc1;
 }
 
-__global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const DecodeParams p)
+// Ask L2 to fetch [p, p + bytes) from HBM (no completion tracking); the lanes
+// of one warp split the range into 4 KB pieces.
+__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes, int lane)
+{
+    const char* c = static_cast<const char*>(p);
+    for (size_t o = (size_t)lane * 4096; o < bytes; o += 32 * 4096) {
+        const size_t n = bytes - o < 4096 ? bytes - o : 4096;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + o), "r"((unsigned)n) : "memory");
+    }
+}
+
+// Tiles in flight per warp: the register ring of prefetched tiles (even).
+constexpr int kRing = 4;
+
+__global__ void __launch_bounds__(kDecodeThreads, 512 / kDecodeThreads) decode_kernel(const DecodeParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* lut = smem;
@@ -185,16 +243,33 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const DecodeP
     float* xs = tbuf + 16 * kPad;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long U = (long long)p.S * p.T;
-    const int u0 = (int)(U * blockIdx.x / gridDim.x);
-    const int u1 = (int)(U * (blockIdx.x + 1) / gridDim.x);
+    // Units owned by this CTA, [u0, u1) in slice-major order.  With
+    // ctas_per_slice > 0 every CTA stays inside one slice (one table build);
+    // otherwise (more slices than CTAs) the units are split evenly.
+    int u0, u1;
+    if (p.ctas_per_slice > 0) {
+        const int s = blockIdx.x / p.ctas_per_slice, c = blockIdx.x - s * p.ctas_per_slice;
+        u0 = s * p.T + (int)((long long)p.T * c / p.ctas_per_slice);
+        u1 = s * p.T + (int)((long long)p.T * (c + 1) / p.ctas_per_slice);
+    } else {
+        const long long U = (long long)p.S * p.T;
+        u0 = (int)(U * blockIdx.x / gridDim.x);
+        u1 = (int)(U * (blockIdx.x + 1) / gridDim.x);
+    }
     const size_t npad = (size_t)p.T * kTileRows;
     // Per-lane part of every table offset: byte 0 for even bytes, byte 1 for odd.
     const uint32_t base_off = (uint32_t)(4 * (lane & 15) + 64 * (lane >> 4)) |
                               ((uint32_t)(4 * (lane & 15) + 64 * (1 - (lane >> 4))) << 8);
 
-    pdl_launch_dependents();
-    bool waited = false;
+    // The weights do not depend on the previous kernel: start streaming this
+    // CTA's whole share (one contiguous range of bits and one of scales) from
+    // HBM into L2 before waiting for it.
+#ifndef BITLIN_NO_L2_PREFETCH
+    if (warp == 0) prefetch_l2(p.bits + (size_t)u0 * 128, (size_t)(u1 - u0) * 2048, lane);
+    if (warp == 1) prefetch_l2(p.scales + (size_t)u0 * 32, (size_t)(u1 - u0) * 256, lane);
+#endif
+    pdl_wait();
+    bool triggered = false;
 
     for (int u = u0; u < u1;) {
         const int s = u / p.T;
@@ -203,55 +278,104 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const DecodeP
         u += tb - ta;
 
         for (int m = 0; m < p.M; ++m) {
-            int t = ta + warp;
-            uint4 cb[4];
-            uint2 cs = make_uint2(0, 0);
-            if (t < tb) load_tile(p, s, t, lane, cb, cs);
-            if (!waited) {
-                pdl_wait();
-                waited = true;
-            }
             __syncthreads();  // the previous table is no longer read
-            build_slice(p, m, s, tbuf, xs, warp, lane);
+            // x first (the slice prologue), then this warp's first tiles
+            // ta + warp + 8j, j < kRing, so that their latency overlaps the
+            // transform and the table build.
+            float xv[4 * kRowsPerWarp];
+            slice_load(p, m, s, warp, lane, xv);
+            uint4 rb[kRing][4];
+            uint2 rs[kRing];
+#pragma unroll
+            for (int d = 0; d < kRing; ++d) {
+                const int t = ta + warp + kDecodeWarps * d;
+                if (t < tb) load_tile(p, s, t, lane, rb[d], rs[d]);
+            }
+            slice_transform(s, xv, tbuf, xs, warp, lane);
             build_tables(xs, lut, warp, lane);
             __syncthreads();
+            // The next kernel may launch now: its weight prefetch then overlaps
+            // this kernel's lookups rather than its latency-bound prologue.
+            if (!triggered) {
+                pdl_launch_dependents();
+                triggered = true;
+            }
             float* part = p.partials + ((size_t)s * p.M + m) * npad;
-            for (; t < tb; t += kDecodeWarps) {
-                const int tn = t + kDecodeWarps;
-                uint4 nb[4];
-                uint2 ns = make_uint2(0, 0);
-                if (tn < tb) load_tile(p, s, tn, lane, nb, ns);
-                part[(size_t)t * kTileRows + lane] = tile_dot(lut, cb, cs, base_off);
-                if (tn < tb) {
+            for (int j0 = 0;; j0 += kRing) {
+                bool more = true;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) cb[q] = nb[q];
-                    cs = ns;
+                for (int d = 0; d < kRing; d += 2) {
+                    const int t0 = ta + warp + kDecodeWarps * (j0 + d);
+                    const int t1 = t0 + kDecodeWarps;
+                    if (t0 >= tb) {
+                        more = false;
+                        break;
+                    }
+                    float v0, v1;
+                    tile_dot2(lut, rb[d], rs[d], rb[d + 1], rs[d + 1], base_off, v0, v1);
+                    const int tn0 = t0 + kDecodeWarps * kRing, tn1 = t1 + kDecodeWarps * kRing;
+                    if (tn0 < tb) load_tile(p, s, tn0, lane, rb[d], rs[d]);
+                    if (tn1 < tb) load_tile(p, s, tn1, lane, rb[d + 1], rs[d + 1]);
+                    part[(size_t)t0 * kTileRows + lane] = v0;
+                    if (t1 < tb) part[(size_t)t1 * kTileRows + lane] = v1;
                 }
+                if (!more) break;
             }
         }
 
-        // Publish this segment's partial sums; the last slice in for a tile
-        // sums all slices of that tile in order and rearms its ticket.
+        // Publish this segment's partial sums, then take one ticket per tile
+        // (all of this warp's tiles at once, one lane each).  The last slice in
+        // for a tile sums all slices of the tile in fixed order and rearms the
+        // ticket.
         __threadfence();
         __syncwarp();
-        for (int t = ta + warp; t < tb; t += kDecodeWarps) {
-            unsigned prev = 0;
-            if (lane == 0) prev = atomicAdd(p.counters + t, 1u);
-            prev = __shfl_sync(0xffffffffu, prev, 0);
-            if (prev == (unsigned)(p.S - 1)) {
-                __threadfence();
-                const int n = t * kTileRows + lane;
-                for (int m = 0; m < p.M; ++m) {
-                    float sum = 0.f;
-                    for (int ss = 0; ss < p.S; ++ss)
-                        sum += __ldcg(p.partials + ((size_t)ss * p.M + m) * npad + n);
-                    if (n < p.N) p.y[(size_t)m * p.N + n] = sum;
+        const int nt = (tb - ta - warp + kDecodeWarps - 1) / kDecodeWarps;  // this warp's tiles
+        for (int j0 = 0; j0 < nt; j0 += 32) {
+            const int j = j0 + lane;
+            bool last = false;
+            if (j < nt)
+                last = atomicAdd(p.counters + (size_t)(ta + warp + kDecodeWarps * j) * kTicketStride, 1u) ==
+                       (unsigned)(p.S - 1);
+            unsigned mask = __ballot_sync(0xffffffffu, last);
+            if (!mask) continue;
+            __threadfence();
+            // Two finished tiles at a time; every partial of a pair is requested
+            // before any is added, and each sum runs over s = 0..S-1.
+            while (mask) {
+                const int ta0 = ta + warp + kDecodeWarps * (j0 + __ffs(mask) - 1);
+                mask &= mask - 1;
+                int ta1 = -1;
+                if (mask) {
+                    ta1 = ta + warp + kDecodeWarps * (j0 + __ffs(mask) - 1);
+                    mask &= mask - 1;
                 }
-                if (lane == 0) p.counters[t] = 0u;
+                for (int m = 0; m < p.M; ++m) {
+                    float sum0 = 0.f, sum1 = 0.f;
+                    for (int s0 = 0; s0 < p.S; s0 += 16) {
+                        float v0[16], v1[16];
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const size_t base = ((size_t)(s0 + k) * p.M + m) * npad + lane;
+                            const bool in = s0 + k < p.S;
+                            v0[k] = in ? __ldcg(p.partials + base + (size_t)ta0 * kTileRows) : 0.f;
+                            v1[k] = (in && ta1 >= 0) ? __ldcg(p.partials + base + (size_t)ta1 * kTileRows) : 0.f;
+                        }
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            sum0 += v0[k];
+                            sum1 += v1[k];
+                        }
+                    }
+                    const int n0 = ta0 * kTileRows + lane, n1 = ta1 * kTileRows + lane;
+                    if (n0 < p.N) p.y[(size_t)m * p.N + n0] = sum0;
+                    if (ta1 >= 0 && n1 < p.N) p.y[(size_t)m * p.N + n1] = sum1;
+                }
+                if (lane == 0) p.counters[(size_t)ta0 * kTicketStride] = 0u;
+                if (lane == 1 && ta1 >= 0) p.counters[(size_t)ta1 * kTicketStride] = 0u;
             }
         }
     }
-    if (!waited) pdl_wait();
+    if (!triggered) pdl_launch_dependents();
 }
 
 }  // namespace
@@ -265,8 +389,16 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const long long U = (long long)p.S * p.T;
-    const int grid = (int)(U < num_sms ? U : num_sms);
+    DecodeParams q = p;
+    int grid;
+    if (p.S <= num_sms) {
+        q.ctas_per_slice = num_sms / p.S < p.T ? num_sms / p.S : p.T;
+        grid = p.S * q.ctas_per_slice;
+    } else {
+        const long long U = (long long)p.S * p.T;
+        q.ctas_per_slice = 0;
+        grid = (int)(U < num_sms ? U : num_sms);
+    }
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -278,5 +410,5 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel, p);
+    return cudaLaunchKernelEx(&cfg, decode_kernel, q);
 }

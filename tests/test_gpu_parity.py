@@ -21,6 +21,7 @@ pytestmark = pytest.mark.gpu
 
 DECODE_TOL = 1e-5
 PREFILL_TOL = 1e-2
+BF16_DIAG_TOL = 1e-3
 
 
 @pytest.fixture(scope="module")
@@ -122,10 +123,12 @@ def test_prefill_full_size_sampled_rows(hrb):
     rows = synth.sample_rows(w.seed, w.N, 160)
     ref = oracle.forward(bits, scales, signs, w.perm, x, rows)
     assert max_rel_l2(y[:, rows], ref) <= PREFILL_TOL
-    # against the oracle with bf16-rounded activations the error is only the
-    # f32 accumulation order
+    # Against the oracle with bf16-rounded activations what remains is the f32
+    # accumulation and the few elements whose rounding to bf16 flips because
+    # the kernel rounds its f32 value and the oracle its f64 value (one bf16
+    # ulp, 2^-8 relative, each): well under 1e-3.
     ref16 = oracle.forward(bits, scales, signs, w.perm, x, rows, round_bf16=True)
-    assert max_rel_l2(y[:, rows], ref16) <= 1e-4
+    assert max_rel_l2(y[:, rows], ref16) <= BF16_DIAG_TOL
     assert np.all(np.isfinite(y))
 
 
@@ -141,7 +144,7 @@ def test_prefill_ragged(hrb, N, K, M, perm):
     ref = oracle.forward(bits, scales, signs, perm, x)
     assert max_rel_l2(y, ref) <= PREFILL_TOL
     ref16 = oracle.forward(bits, scales, signs, perm, x, round_bf16=True)
-    assert max_rel_l2(y, ref16) <= 1e-4
+    assert max_rel_l2(y, ref16) <= BF16_DIAG_TOL
 
 
 # ------------------------------------------------------------------ edge cases
