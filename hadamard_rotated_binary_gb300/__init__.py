@@ -15,6 +15,7 @@ from __future__ import annotations
 
 from ._binding import (  # noqa: F401
     BITLIN_EDEVICE,
+    BITLIN_ESCRATCH,
     BITLIN_EINVAL,
     BITLIN_ENOMEM,
     BITLIN_ECUDA,

@@ -15,6 +15,7 @@ BITLIN_ENOMEM = 2
 BITLIN_ECUDA = 3
 BITLIN_ETIMEOUT = 4
 BITLIN_EDEVICE = 5
+BITLIN_ESCRATCH = 6
 
 PERM_NONE = 0
 PERM_SSM_TILED_TO_GROUPED = 1
@@ -59,6 +60,9 @@ def lib() -> ctypes.CDLL:
     L.bitlin_create.argtypes = [ctypes.POINTER(P), i32, i32, P, P, P, i32]
     L.bitlin_forward.argtypes = [P, P, i32, P, P]
     L.bitlin_forward_host.argtypes = [P, P, i32, P, P]
+    L.bitlin_forward_noalloc.argtypes = [P, P, i32, P, P]
+    L.bitlin_forward_noalloc.restype = i32
+    L.bitlin_noalloc_scratch_bytes.restype = ctypes.c_size_t
     L.bitlin_set_path.argtypes = [P, i32]
     L.bitlin_set_wait_budget.argtypes = [P, i64]
     L.bitlin_test_stall.argtypes = [P, i32]
@@ -146,6 +150,13 @@ class BitLinear:
         self._check(lib().bitlin_forward_host(self._h, x_host.ctypes.data, M, y_host.ctypes.data,
                                               _stream_handle(stream)), "bitlin_forward_host")
         return y_host
+
+    def forward_noalloc(self, x, out, stream=None):
+        """bitlin_forward_noalloc: y into `out` with the library's fixed scratch (no allocation)."""
+        M = int(x.shape[0])
+        self._check(lib().bitlin_forward_noalloc(self._h, x.data_ptr(), M, out.data_ptr(),
+                                                 _stream_handle(stream)), "bitlin_forward_noalloc")
+        return out
 
     def set_path(self, path: int):
         self._check(lib().bitlin_set_path(self._h, int(path)), "bitlin_set_path")

@@ -158,6 +158,7 @@ const char* bitlin_status_string(bitlin_status s)
     case BITLIN_ECUDA: return "CUDA runtime error";
     case BITLIN_ETIMEOUT: return "a bounded device wait timed out";
     case BITLIN_EDEVICE: return "the current device is not an sm_103 GPU";
+    case BITLIN_ESCRATCH: return "the call needs more scratch than the fixed no-alloc array holds";
     }
     return "unknown status";
 }

@@ -56,7 +56,8 @@ typedef enum {
     BITLIN_ENOMEM = 2,   /* a device or host allocation failed */
     BITLIN_ECUDA = 3,    /* a CUDA runtime call or kernel launch failed (see bitlin_cuda_error) */
     BITLIN_ETIMEOUT = 4, /* a bounded wait inside a kernel gave up; the output is not valid */
-    BITLIN_EDEVICE = 5   /* the current device is not an sm_103 GPU */
+    BITLIN_EDEVICE = 5,  /* the current device is not an sm_103 GPU */
+    BITLIN_ESCRATCH = 6  /* bitlin_forward_noalloc: the call needs more than its fixed scratch */
 } bitlin_status;
 
 #define BITLIN_PERM_NONE 0
@@ -114,6 +115,40 @@ bitlin_status bitlin_forward(bitlin_t h, const float* x, int M, float* y, bitlin
  */
 bitlin_status bitlin_forward_host(bitlin_t h, const float* x_host, int M, float* y_host,
                                   bitlin_stream_t stream);
+
+/*
+ * bitlin_forward for callers that must not allocate device memory on their
+ * call path: code running inside a runtime that owns every device
+ * allocation (a memory pool or arena that forbids outside cudaMalloc), and
+ * latency-critical loops that must never enter the allocator, since cudaMalloc
+ * and cudaFree can synchronize the whole device.  bitlin_forward may grow the
+ * handle's scratch on a call with a new largest M; this entry point never
+ * allocates.  It has no counterpart on the pages; it is an interface choice of
+ * this library.
+ *
+ * Computes the same y[M][N] with the f32 decode GEMV (for every M), reading
+ * x and writing y (device pointers, as bitlin_forward) on `stream`.  Its
+ * split-K scratch is a fixed array of bitlin_noalloc_scratch_bytes() bytes
+ * (16 MiB) compiled into the library, which every GPU that loads the library
+ * keeps until the process exits.  The call needs
+ *     align256(ceil(N/32) * 128) + (K/512) * M * ceil(N/32) * 128  bytes
+ * of it and returns BITLIN_ESCRATCH, launching nothing, when that exceeds the
+ * array (for example M=1 fits up to N = 248,320 at K = 5120).
+ * The first call on a device, with that device current, looks up the array's
+ * device address (cudaGetSymbolAddress) and caches it: make that first call
+ * before any stream capture.  Every call shares the array, which keeps the
+ * previous call's contents; each call clears the part that must start at zero
+ * with cudaMemsetAsync on `stream`.  Calls whose kernels overlap on the GPU
+ * (different streams, or several host threads) race on the array: serialize
+ * them.
+ * Errors: BITLIN_EINVAL (NULL handle/x/y, M < 1, current device differs from
+ * the handle's), BITLIN_ESCRATCH, BITLIN_ECUDA, and the handle's sticky error.
+ */
+bitlin_status bitlin_forward_noalloc(bitlin_t h, const float* x, int M, float* y,
+                                     bitlin_stream_t stream);
+
+/* Size in bytes of the fixed scratch array used by bitlin_forward_noalloc. */
+size_t bitlin_noalloc_scratch_bytes(void);
 
 /* Select the path used for later calls (BITLIN_PATH_*).  EINVAL on an unknown value. */
 bitlin_status bitlin_set_path(bitlin_t h, int path);
