@@ -356,8 +356,8 @@ def main():
         "hbm_frac_of_8tbs": achieved / 8000.0,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "peak_kind": peak_kind,
-                     "kernel": "decode_kernel", "bytes_per_launch": algo_bytes,
-                     "traffic": traffic_record("decode_kernel", w.name)},
+                     "kernel": "bitlin_decode_gemv", "bytes_per_launch": algo_bytes,
+                     "traffic": traffic_record("bitlin_decode_gemv", w.name)},
         "gpu_launches": args.steps * (1 if w.M < 64 else 2),
         "clocks": clocks,
         "e2e": {"value": ws * w.M * e2e_steps / e2e_s, "unit": UNIT,

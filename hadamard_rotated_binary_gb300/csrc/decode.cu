@@ -235,7 +235,7 @@ __device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes, int lan
 // Tiles in flight per warp: the register ring of prefetched tiles (even).
 constexpr int kRing = 4;
 
-__global__ void __launch_bounds__(kDecodeThreads, 512 / kDecodeThreads) decode_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(kDecodeThreads, 512 / kDecodeThreads) bitlin_decode_gemv(const DecodeParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* lut = smem;
@@ -384,7 +384,7 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
 {
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(bitlin_decode_gemv, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kDecodeSmem);
         if (e != cudaSuccess) return e;
         configured = true;
@@ -410,5 +410,5 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel, q);
+    return cudaLaunchKernelEx(&cfg, bitlin_decode_gemv, q);
 }

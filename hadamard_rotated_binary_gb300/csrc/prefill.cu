@@ -62,7 +62,7 @@ struct __align__(8) Barriers {
 constexpr int kSmemBytes = 2 * kPrefillStages * kStageBytes + (int)sizeof(Barriers) + 1024;
 
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmap_xt, const PrefillParams p, int stall_test)
+    bitlin_tc_gemm(const __grid_constant__ CUtensorMap tmap_xt, const PrefillParams p, int stall_test)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -248,13 +248,13 @@ cudaError_t bitlin_launch_prefill(const PrefillParams& p, const void* tmap, int 
 {
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(bitlin_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     dim3 grid((p.N + kPrefillRows - 1) / kPrefillRows, (p.M + kPrefillTokens - 1) / kPrefillTokens);
-    prefill_kernel<<<grid, kThreads, kSmemBytes, s>>>(*static_cast<const CUtensorMap*>(tmap), p,
+    bitlin_tc_gemm<<<grid, kThreads, kSmemBytes, s>>>(*static_cast<const CUtensorMap*>(tmap), p,
                                                       stall_test);
     return cudaGetLastError();
 }

@@ -26,7 +26,7 @@ namespace {
 
 using namespace bitlin_impl;
 
-__global__ void repack_decode_kernel(const uint32_t* __restrict__ bits,
+__global__ void bitlin_repack_decode(const uint32_t* __restrict__ bits,
                                      const uint16_t* __restrict__ scales, int N, int K, int T,
                                      uint4* __restrict__ dbits, uint2* __restrict__ dscales)
 {
@@ -78,14 +78,14 @@ __device__ __forceinline__ uint32_t unshuffle_bits(uint32_t v)
     return r;
 }
 
-__global__ void repack_prefill_kernel(const uint32_t* __restrict__ bits, long long words,
+__global__ void bitlin_repack_tc(const uint32_t* __restrict__ bits, long long words,
                                       uint32_t* __restrict__ pbits)
 {
     const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (gid < words) pbits[gid] = unshuffle_bits(bits[gid]);
 }
 
-__global__ void check_signs_kernel(const float* __restrict__ signs, int K, int* bad)
+__global__ void bitlin_check_signs(const float* __restrict__ signs, int K, int* bad)
 {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < K) {
@@ -103,7 +103,7 @@ cudaError_t bitlin_launch_repack_decode(const uint32_t* bits, const uint16_t* sc
     const long long total = (long long)(K / kSlice) * T * 32;
     const int threads = 256;
     const long long blocks = (total + threads - 1) / threads;
-    repack_decode_kernel<<<(unsigned)blocks, threads, 0, s>>>(bits, scales, N, K, T, dbits, dscales);
+    bitlin_repack_decode<<<(unsigned)blocks, threads, 0, s>>>(bits, scales, N, K, T, dbits, dscales);
     return cudaGetLastError();
 }
 
@@ -113,12 +113,12 @@ cudaError_t bitlin_launch_repack_prefill(const uint32_t* bits, int N, int K, uin
     const long long words = (long long)N * (K / 32);
     const int threads = 256;
     const long long blocks = (words + threads - 1) / threads;
-    repack_prefill_kernel<<<(unsigned)blocks, threads, 0, s>>>(bits, words, pbits);
+    bitlin_repack_tc<<<(unsigned)blocks, threads, 0, s>>>(bits, words, pbits);
     return cudaGetLastError();
 }
 
 cudaError_t bitlin_launch_check_signs(const float* signs, int K, int* bad, cudaStream_t s)
 {
-    check_signs_kernel<<<(K + 255) / 256, 256, 0, s>>>(signs, K, bad);
+    bitlin_check_signs<<<(K + 255) / 256, 256, 0, s>>>(signs, K, bad);
     return cudaGetLastError();
 }

@@ -22,7 +22,7 @@ __device__ __forceinline__ int perm_source(int k)
     return d + 128 * (kk + 16 * r);
 }
 
-__global__ void __launch_bounds__(256) rotate_bf16_kernel(const float* __restrict__ x,
+__global__ void __launch_bounds__(256) bitlin_rotate_bf16(const float* __restrict__ x,
                                                           const float* __restrict__ signs, int M,
                                                           int K, int perm,
                                                           __nv_bfloat16* __restrict__ xt)
@@ -73,7 +73,7 @@ cudaError_t bitlin_launch_rotate_bf16(const float* x, const float* signs, int M,
     const long long warps = (long long)M * (K / 1024);
     const int threads = 256;
     const long long blocks = (warps * 32 + threads - 1) / threads;
-    rotate_bf16_kernel<<<(unsigned)blocks, threads, 0, s>>>(x, signs, M, K, perm,
+    bitlin_rotate_bf16<<<(unsigned)blocks, threads, 0, s>>>(x, signs, M, K, perm,
                                                            static_cast<__nv_bfloat16*>(xt));
     return cudaGetLastError();
 }
