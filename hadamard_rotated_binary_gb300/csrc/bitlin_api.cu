@@ -219,8 +219,8 @@ bitlin_status bitlin_create(bitlin_t* out, int N, int K, const uint32_t* packed_
     BITLIN_TRY(cudaMalloc(&h->dev_error, 2 * sizeof(int)));
     BITLIN_TRY(cudaHostAlloc(&h->h_err, sizeof(int), cudaHostAllocDefault));
     bad = h->dev_error + 1;
-    BITLIN_TRY(cudaMemsetAsync(h->counters, 0, (size_t)h->T * kTicketStride * sizeof(unsigned), st));
     BITLIN_TRY(cudaMemsetAsync(h->dev_error, 0, 2 * sizeof(int), st));
+    BITLIN_TRY(cudaMemsetAsync(h->counters, 0, (size_t)h->T * kTicketStride * sizeof(unsigned), st));
     BITLIN_TRY(cudaMemcpyAsync(h->signs, signs, (size_t)K * sizeof(float), cudaMemcpyDeviceToDevice, st));
     BITLIN_TRY(cudaMemcpyAsync(h->pscales, scales, groups * sizeof(uint16_t), cudaMemcpyDeviceToDevice, st));
     BITLIN_TRY(bitlin_launch_check_signs(h->signs, K, bad, st));

@@ -16,9 +16,9 @@ constexpr int kTileRows = 32;         // rows per tile (one row per lane)
 constexpr int kWordsPerSlice = 16;    // uint32 words of one row in one slice
 constexpr int kGroupsPerSlice = 4;    // 128-weight scale groups per slice
 #ifndef BITLIN_DECODE_THREADS
-#define BITLIN_DECODE_THREADS 256
+#define BITLIN_DECODE_THREADS 512
 #endif
-constexpr int kDecodeThreads = BITLIN_DECODE_THREADS;  // 8 warps per CTA: two CTAs fit on an SM
+constexpr int kDecodeThreads = BITLIN_DECODE_THREADS;  // 16 warps per CTA, one CTA per SM
 constexpr int kDecodeWarps = kDecodeThreads / 32;
 constexpr int kLutBytes = 65536;      // 64 octet tables x 256 entries x f32
 constexpr int kTicketStride = 32;     // one split-K ticket per 128-byte line
@@ -38,8 +38,8 @@ struct DecodeParams {
     const float* signs;     // [K]
     const float* x;         // [M][K]
     float* y;               // [M][N]
-    float* partials;        // [S][M][T*32]
-    unsigned* counters;     // [T * kTicketStride], zero between calls
+    float* partials;        // [S][M][T*32], fully rewritten by every call
+    unsigned* counters;     // [T * kTicketStride] split-K tickets, zero between calls
     int M, N, K, S, T, perm;
     int ctas_per_slice;     // set by the launcher
 };

@@ -8,10 +8,12 @@
 //
 // How (GB300 design):
 //  * Work unit = (slice s of 512 weights along K) x (tile t of 32 rows).  A CTA
-//    (8 warps, one per SM) takes a contiguous run of units, so it touches one
-//    or two slices; split-K partial sums land in a scratch array and the last
-//    contributor of each tile (an atomic ticket per tile) adds the slices in
-//    fixed order s = 0..S-1 - deterministic results.
+//    (8 warps, one per SM) owns one slice and a contiguous range of tiles.
+//    Split-K partial sums land in a scratch array; at the end each CTA takes
+//    one ticket per tile in parallel, and the CTA that draws the last ticket
+//    of a tile sums its S partials in fixed order s = 0..S-1 (deterministic)
+//    with all of its threads.  One kernel per call, so that programmatic
+//    dependent launch can overlap consecutive calls.
 //  * Prologue per (token, slice): gather x (with the ssm_out permutation when
 //    requested), multiply by the signs, and form the 512 outputs of the
 //    1024-point transform that the slice needs: with H1024 = [[H, H], [H, -H]],
@@ -52,7 +54,8 @@ using namespace bitlin_impl;
 constexpr int kPad = 33;                               // transpose row stride (floats)
 constexpr int kSmemTranspose = 16 * kPad * 4;           // 2112 B
 constexpr int kSmemSlice = (kSlice + kSlice / 32) * 4;  // 528 floats
-constexpr int kDecodeSmem = kLutBytes + kSmemTranspose + kSmemSlice;
+constexpr int kMaxList = 1024;                          // finished-tile list (ints)
+constexpr int kDecodeSmem = kLutBytes + kSmemTranspose + kSmemSlice + (kMaxList + 1) * 4;
 constexpr int kRowsPerWarp = 16 / kDecodeWarps;  // rows of the [16][32] transform view per warp
 static_assert(kDecodeWarps == 8 || kDecodeWarps == 16, "prologue mapping assumes 8 or 16 warps");
 
@@ -113,10 +116,12 @@ __device__ __forceinline__ void slice_load(const DecodeParams& p, int m, int s, 
 }
 
 // slice_transform: half h of the block's 1024-point transform is
-// H512(xs_lo + (-1)^h xs_hi) / 32 with H512 = H16 (x) H32; the result goes to xs
-// (padded, 512 floats).
-__device__ __forceinline__ void slice_transform(int s, const float (&v)[4 * kRowsPerWarp], float* tbuf, float* xs,
-                                                int warp, int lane)
+// H512(xs_lo + (-1)^h xs_hi) / 32 with H512 = H16 (x) H32.  Rows part: the
+// 32-point butterflies across the lanes, into tbuf; the caller then
+// synchronizes and runs the columns part (16-point butterflies across
+// half-warps, x 1/32, into xs, padded, 512 floats).
+__device__ __forceinline__ void slice_transform_rows(int s, const float (&v)[4 * kRowsPerWarp], float* tbuf,
+                                                     int warp, int lane)
 {
     const int h = s & 1;
 #pragma unroll
@@ -132,7 +137,10 @@ __device__ __forceinline__ void slice_transform(int s, const float (&v)[4 * kRow
         }
         tbuf[(warp + kDecodeWarps * r) * kPad + lane] = z;
     }
-    __syncthreads();
+}
+
+__device__ __forceinline__ void slice_transform_cols(const float* tbuf, float* xs, int warp, int lane)
+{
     // 16-point butterflies down the columns: warp w takes 32 / warps columns,
     // one per half-warp and round; lane & 15 is the row.
     const int row = lane & 15;
@@ -147,7 +155,6 @@ __device__ __forceinline__ void slice_transform(int s, const float (&v)[4 * kRow
         }
         xs[xpad(row * 32 + col)] = z * 0.03125f;  // exact scaling by 1/32
     }
-    __syncthreads();
 }
 
 // Signed-sum tables for the slice: warp v writes entries b = 16*hn .. 16*hn+15
@@ -221,13 +228,14 @@ __device__ __forceinline__ void tile_dot2(const unsigned char* lut, const uint4 
     out1 = acc1;
 }
 
-// Ask L2 to fetch [p, p + bytes) from HBM (no completion tracking); the lanes
-// of one warp split the range into 4 KB pieces.
-__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes, int lane)
+// Ask L2 to fetch [p, p + bytes) from HBM (no completion tracking), in 16 KB
+// pieces spread over the CTA's threads so that no warp spends long issuing.
+__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes, int tid)
 {
     const char* c = static_cast<const char*>(p);
-    for (size_t o = (size_t)lane * 4096; o < bytes; o += 32 * 4096) {
-        const size_t n = bytes - o < 4096 ? bytes - o : 4096;
+    constexpr size_t kPiece = 16384;
+    for (size_t o = (size_t)tid * kPiece; o < bytes; o += (size_t)kDecodeThreads * kPiece) {
+        const size_t n = bytes - o < kPiece ? bytes - o : kPiece;
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + o), "r"((unsigned)n) : "memory");
     }
 }
@@ -235,12 +243,103 @@ __device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes, int lan
 // Tiles in flight per warp: the register ring of prefetched tiles (even).
 constexpr int kRing = 4;
 
-__global__ void __launch_bounds__(kDecodeThreads, 512 / kDecodeThreads) bitlin_decode_gemv(const DecodeParams p)
+// Registers per thread: with 8 warps per CTA two CTAs (this call's and the
+// next call's) fit in an SM's 65,536 registers.
+constexpr int kDecodeRegs = 128;
+
+// End of a segment [ta, tb) of one slice: publish the partial sums, take one
+// ticket per tile (in parallel, one thread each), and reduce the tiles whose
+// S-th ticket this CTA drew: every output row of those tiles is the sum of its
+// S partials in slice order s = 0..S-1 (deterministic).
+// Ordering: the tickets are acquire-release atomics taken after a CTA barrier
+// and followed by one, so the partial stores of every slice happen before the
+// loads of whichever CTA completes a tile.  The finished tiles' partials are staged into shared memory
+// (the table area, free by then) with asynchronous 16-byte copies, all in
+// flight at once, then summed in slice order.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+
+// One split-K ticket: atomic increment at GPU scope with release semantics
+// (the CTA's partial stores, ordered before it by the preceding barrier, are
+// visible to whoever observes the increment) and acquire semantics (the
+// partials of the other slices, released by their tickets, are visible to
+// this CTA's loads after the following barrier).
+__device__ __forceinline__ unsigned ticket_acq_rel(unsigned* addr)
+{
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(addr) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void splitk_finish(const DecodeParams& p, int ta, int tb, size_t npad,
+                                              int* done_list, int* done_count, float* stage)
+{
+    __syncthreads();  // every partial store is done, and every warp is done reading the tables
+    const int ntiles = tb - ta;
+    const int per_batch = kLutBytes / (p.S * kTileRows * 4);  // tiles whose S partials fit
+    for (int base = 0; base < ntiles; base += kMaxList) {
+        const int chunk = min(kMaxList, ntiles - base);
+        if (threadIdx.x == 0) *done_count = 0;
+        __syncthreads();
+        for (int i = threadIdx.x; i < chunk; i += kDecodeThreads) {
+            const int t = ta + base + i;
+            if (ticket_acq_rel(p.counters + (size_t)t * kTicketStride) == (unsigned)(p.S - 1)) {
+                p.counters[(size_t)t * kTicketStride] = 0u;  // rearm for the next call
+                done_list[atomicAdd(done_count, 1)] = t;
+            }
+        }
+        __syncthreads();
+        const int ndone = *done_count;
+        for (int m = 0; m < p.M; ++m) {
+            for (int b0 = 0; b0 < ndone; b0 += per_batch) {
+                const int nb = min(per_batch, ndone - b0);
+                const int pieces = p.S * nb * (kTileRows / 4);  // 16-byte pieces
+                for (int c = threadIdx.x; c < pieces; c += kDecodeThreads) {
+                    const int sl = c / (nb * 8), rem = c - sl * nb * 8;
+                    const int ti = rem >> 3, q = rem & 7;
+                    const float* src = p.partials + ((size_t)sl * p.M + m) * npad +
+                                       (size_t)done_list[b0 + ti] * kTileRows + 4 * q;
+                    cp_async16(stage + ((size_t)sl * nb + ti) * kTileRows + 4 * q, src);
+                }
+                asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+                __syncthreads();
+                for (int r = threadIdx.x; r < nb * kTileRows; r += kDecodeThreads) {
+                    const int ti = r >> 5, lane = r & 31;
+                    const float* col = stage + (size_t)ti * kTileRows + lane;
+                    const int sstep = nb * kTileRows;
+                    float sum = 0.f;
+                    int sl = 0;
+                    for (; sl + 4 <= p.S; sl += 4) {
+                        const float a = col[(size_t)sl * sstep], b = col[(size_t)(sl + 1) * sstep];
+                        const float c = col[(size_t)(sl + 2) * sstep], d = col[(size_t)(sl + 3) * sstep];
+                        sum += a;
+                        sum += b;
+                        sum += c;
+                        sum += d;
+                    }
+                    for (; sl < p.S; ++sl) sum += col[(size_t)sl * sstep];
+                    const int n = done_list[b0 + ti] * kTileRows + lane;
+                    if (n < p.N) p.y[(size_t)m * p.N + n] = sum;
+                }
+                __syncthreads();  // the stage is refilled by the next batch
+            }
+        }
+    }
+}
+
+__global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* lut = smem;
     float* tbuf = reinterpret_cast<float*>(smem + kLutBytes);
     float* xs = tbuf + 16 * kPad;
+    int* done_list = reinterpret_cast<int*>(xs + kSlice + kSlice / 32);  // [kMaxList]
+    int* done_count = done_list + kMaxList;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Units owned by this CTA, [u0, u1) in slice-major order.  With
@@ -265,8 +364,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 512 / kDecodeThreads) bitlin_d
     // CTA's whole share (one contiguous range of bits and one of scales) from
     // HBM into L2 before waiting for it.
 #ifndef BITLIN_NO_L2_PREFETCH
-    if (warp == 0) prefetch_l2(p.bits + (size_t)u0 * 128, (size_t)(u1 - u0) * 2048, lane);
-    if (warp == 1) prefetch_l2(p.scales + (size_t)u0 * 32, (size_t)(u1 - u0) * 256, lane);
+    prefetch_l2(p.bits + (size_t)u0 * 128, (size_t)(u1 - u0) * 2048, threadIdx.x);
+    prefetch_l2(p.scales + (size_t)u0 * 32, (size_t)(u1 - u0) * 256, (threadIdx.x + 128) % kDecodeThreads);
 #endif
     pdl_wait();
     bool triggered = false;
@@ -279,11 +378,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 512 / kDecodeThreads) bitlin_d
 
         for (int m = 0; m < p.M; ++m) {
             __syncthreads();  // the previous table is no longer read
-            // x first (the slice prologue), then this warp's first tiles
-            // ta + warp + 8j, j < kRing, so that their latency overlaps the
-            // transform and the table build.
+            // x first, alone, so that its loads are not queued behind the tile
+            // loads; then this warp's first tiles ta + warp + 8j, j < kRing,
+            // whose latency overlaps the transform and the table build.
             float xv[4 * kRowsPerWarp];
             slice_load(p, m, s, warp, lane, xv);
+            slice_transform_rows(s, xv, tbuf, warp, lane);
             uint4 rb[kRing][4];
             uint2 rs[kRing];
 #pragma unroll
@@ -291,7 +391,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 512 / kDecodeThreads) bitlin_d
                 const int t = ta + warp + kDecodeWarps * d;
                 if (t < tb) load_tile(p, s, t, lane, rb[d], rs[d]);
             }
-            slice_transform(s, xv, tbuf, xs, warp, lane);
+            __syncthreads();
+            slice_transform_cols(tbuf, xs, warp, lane);
+            __syncthreads();
             build_tables(xs, lut, warp, lane);
             __syncthreads();
             // The next kernel may launch now: its weight prefetch then overlaps
@@ -322,58 +424,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 512 / kDecodeThreads) bitlin_d
                 if (!more) break;
             }
         }
-
-        // Publish this segment's partial sums, then take one ticket per tile
-        // (all of this warp's tiles at once, one lane each).  The last slice in
-        // for a tile sums all slices of the tile in fixed order and rearms the
-        // ticket.
-        __threadfence();
-        __syncwarp();
-        const int nt = (tb - ta - warp + kDecodeWarps - 1) / kDecodeWarps;  // this warp's tiles
-        for (int j0 = 0; j0 < nt; j0 += 32) {
-            const int j = j0 + lane;
-            bool last = false;
-            if (j < nt)
-                last = atomicAdd(p.counters + (size_t)(ta + warp + kDecodeWarps * j) * kTicketStride, 1u) ==
-                       (unsigned)(p.S - 1);
-            unsigned mask = __ballot_sync(0xffffffffu, last);
-            if (!mask) continue;
-            __threadfence();
-            // Two finished tiles at a time; every partial of a pair is requested
-            // before any is added, and each sum runs over s = 0..S-1.
-            while (mask) {
-                const int ta0 = ta + warp + kDecodeWarps * (j0 + __ffs(mask) - 1);
-                mask &= mask - 1;
-                int ta1 = -1;
-                if (mask) {
-                    ta1 = ta + warp + kDecodeWarps * (j0 + __ffs(mask) - 1);
-                    mask &= mask - 1;
-                }
-                for (int m = 0; m < p.M; ++m) {
-                    float sum0 = 0.f, sum1 = 0.f;
-                    for (int s0 = 0; s0 < p.S; s0 += 16) {
-                        float v0[16], v1[16];
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            const size_t base = ((size_t)(s0 + k) * p.M + m) * npad + lane;
-                            const bool in = s0 + k < p.S;
-                            v0[k] = in ? __ldcg(p.partials + base + (size_t)ta0 * kTileRows) : 0.f;
-                            v1[k] = (in && ta1 >= 0) ? __ldcg(p.partials + base + (size_t)ta1 * kTileRows) : 0.f;
-                        }
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            sum0 += v0[k];
-                            sum1 += v1[k];
-                        }
-                    }
-                    const int n0 = ta0 * kTileRows + lane, n1 = ta1 * kTileRows + lane;
-                    if (n0 < p.N) p.y[(size_t)m * p.N + n0] = sum0;
-                    if (ta1 >= 0 && n1 < p.N) p.y[(size_t)m * p.N + n1] = sum1;
-                }
-                if (lane == 0) p.counters[(size_t)ta0 * kTicketStride] = 0u;
-                if (lane == 1 && ta1 >= 0) p.counters[(size_t)ta1 * kTicketStride] = 0u;
-            }
-        }
+        splitk_finish(p, ta, tb, npad, done_list, done_count, reinterpret_cast<float*>(lut));
     }
     if (!triggered) pdl_launch_dependents();
 }
@@ -400,14 +451,15 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
         grid = (int)(U < num_sms ? U : num_sms);
     }
 
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kDecodeThreads);
     cfg.dynamicSmemBytes = kDecodeSmem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, bitlin_decode_gemv, q);

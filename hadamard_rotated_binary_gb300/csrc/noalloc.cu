@@ -16,9 +16,10 @@
 // device, with that device current, looks the address up with
 // cudaGetSymbolAddress and caches it; make that first call before any stream
 // capture.  All calls share the array and it keeps the previous call's
-// contents: every call clears the split-K tickets it uses before launching,
-// and two calls whose kernels overlap on the GPU (different streams, or
-// concurrent host threads) race on it.
+// contents: every call clears the split-K tickets it uses (cudaMemsetAsync on
+// its stream) before launching; the partial sums need no clearing, each call
+// writes all of them before they are read.  Two calls whose kernels overlap
+// on the GPU (different streams, or concurrent host threads) race on it.
 #include <cuda_runtime.h>
 
 #include <mutex>

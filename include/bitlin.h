@@ -138,9 +138,9 @@ bitlin_status bitlin_forward_host(bitlin_t h, const float* x_host, int M, float*
  * device address (cudaGetSymbolAddress) and caches it: make that first call
  * before any stream capture.  Every call shares the array, which keeps the
  * previous call's contents; each call clears the part that must start at zero
- * with cudaMemsetAsync on `stream`.  Calls whose kernels overlap on the GPU
- * (different streams, or several host threads) race on the array: serialize
- * them.
+ * (its split-K tickets) with cudaMemsetAsync on `stream`.  Calls whose kernels
+ * overlap on the GPU (different streams, or several host threads) race on the
+ * array: serialize them.
  * Errors: BITLIN_EINVAL (NULL handle/x/y, M < 1, current device differs from
  * the handle's), BITLIN_ESCRATCH, BITLIN_ECUDA, and the handle's sticky error.
  */
