@@ -358,7 +358,7 @@ def main():
                      "frac": achieved / peaks["hbm_gbs"], "peak_kind": peak_kind,
                      "kernel": "bitlin_decode_gemv", "bytes_per_launch": algo_bytes,
                      "traffic": traffic_record("bitlin_decode_gemv", w.name)},
-        "gpu_launches": args.steps * (1 if w.M < 64 else 2),  # decode: one GEMV; M >= 64: rotate + GEMM
+        "gpu_launches": args.steps * (1 if w.M == 1 else 2),  # M = 1: one GEMV; else rotate + GEMM
         "clocks": clocks,
         "e2e": {"value": ws * w.M * e2e_steps / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": 4 * w.M * w.K, "d2h_bytes_per_step": 4 * w.M * w.N,

@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     PATH_AUTO,
     PATH_DECODE,
     PATH_PREFILL,
+    PATH_TC_EXACT,
     PERM_NONE,
     PERM_SSM_TILED_TO_GROUPED,
     BitlinError,
@@ -42,6 +43,7 @@ __all__ = [
     "PATH_AUTO",
     "PATH_DECODE",
     "PATH_PREFILL",
+    "PATH_TC_EXACT",
     "PERM_NONE",
     "PERM_SSM_TILED_TO_GROUPED",
 ]

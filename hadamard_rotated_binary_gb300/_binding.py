@@ -22,6 +22,7 @@ PERM_SSM_TILED_TO_GROUPED = 1
 PATH_AUTO = 0
 PATH_DECODE = 1
 PATH_PREFILL = 2
+PATH_TC_EXACT = 3
 
 _lib = None
 

@@ -75,23 +75,25 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
     return fn;
 }
 
-// Rotated-activation buffer (bf16 [M][K]) and its TMA descriptor.
-bitlin_status ensure_xt(bitlin_t h, int M)
+// Rotated-activation buffer for the tensor-core paths and its TMA descriptor:
+// bf16 [M][K] (prefill) or [4M][K] (exact: three digits and a zero row per token).
+bitlin_status ensure_xt(bitlin_t h, int M, int exact)
 {
-    if (!h->xt || h->xt_M < M) {
+    const int rows = exact ? 4 * M : M;
+    if (!h->xt || h->xt_M < rows) {
         free_dev(h->xt);
         h->xt_M = 0;
         h->tmap_M = 0;
-        cudaError_t e = cudaMalloc(&h->xt, (size_t)M * h->K * 2);
+        cudaError_t e = cudaMalloc(&h->xt, (size_t)rows * h->K * 2);
         if (e != cudaSuccess) return from_cuda(h, e);
-        h->xt_M = M;
+        h->xt_M = rows;
     }
-    if (h->tmap_M != M) {
+    if (h->tmap_M != M || h->tmap_exact != exact) {
         PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
         if (!enc) return from_cuda(h, cudaErrorNotSupported);
-        cuuint64_t dims[2] = {(cuuint64_t)h->K, (cuuint64_t)M};
+        cuuint64_t dims[2] = {(cuuint64_t)h->K, (cuuint64_t)rows};
         cuuint64_t strides[1] = {(cuuint64_t)h->K * 2};
-        cuuint32_t box[2] = {64, (cuuint32_t)kPrefillTokens};
+        cuuint32_t box[2] = {64, (cuuint32_t)bitlin_tc_tile_width(M, exact)};
         cuuint32_t estr[2] = {1, 1};
         CUresult r = enc(reinterpret_cast<CUtensorMap*>(h->tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                          h->xt, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -99,6 +101,7 @@ bitlin_status ensure_xt(bitlin_t h, int M)
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return from_cuda(h, cudaErrorInvalidValue);
         h->tmap_M = M;
+        h->tmap_exact = exact;
     }
     return BITLIN_OK;
 }
@@ -124,11 +127,11 @@ bitlin_status run_decode(bitlin_t h, const float* x, int M, float* y, cudaStream
     return from_cuda(h, bitlin_launch_decode(p, h->num_sms, s));
 }
 
-bitlin_status run_prefill(bitlin_t h, const float* x, int M, float* y, cudaStream_t s)
+bitlin_status run_tc(bitlin_t h, const float* x, int M, float* y, cudaStream_t s, int exact)
 {
-    bitlin_status st = ensure_xt(h, M);
+    bitlin_status st = ensure_xt(h, M, exact);
     if (st != BITLIN_OK) return st;
-    cudaError_t e = bitlin_launch_rotate_bf16(x, h->signs, M, h->K, h->perm, h->xt, s);
+    cudaError_t e = bitlin_launch_rotate_bf16(x, h->signs, M, h->K, h->perm, exact, h->xt, s);
     if (e != cudaSuccess) return from_cuda(h, e);
     PrefillParams p;
     p.bits = h->pbits;
@@ -139,7 +142,8 @@ bitlin_status run_prefill(bitlin_t h, const float* x, int M, float* y, cudaStrea
     p.N = h->N;
     p.K = h->K;
     p.wait_budget_ns = h->wait_budget_ns;
-    e = bitlin_launch_prefill(p, h->tmap, h->stall_test, s);
+    e = exact ? bitlin_launch_tc_exact(p, h->tmap, h->tmap_bits, h->stall_test, s)
+              : bitlin_launch_prefill(p, h->tmap, h->tmap_bits, h->stall_test, s);
     return from_cuda(h, e);
 }
 
@@ -230,6 +234,26 @@ bitlin_status bitlin_create(bitlin_t* out, int N, int K, const uint32_t* packed_
     BITLIN_TRY(cudaStreamSynchronize(st));
     cudaStreamDestroy(st);
     st = nullptr;
+    {
+        // Tensor-path bits as a [N][K/32] u32 tensor, read in boxes of 4 words x 128 rows.
+        PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+        if (!enc) {
+            e = cudaErrorNotSupported;
+            goto fail_cuda;
+        }
+        cuuint64_t dims[2] = {(cuuint64_t)(K / 32), (cuuint64_t)N};
+        cuuint64_t strides[1] = {(cuuint64_t)(K / 8)};
+        cuuint32_t box[2] = {4, (cuuint32_t)kPrefillRows};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult r = enc(reinterpret_cast<CUtensorMap*>(h->tmap_bits), CU_TENSOR_MAP_DATA_TYPE_UINT32, 2,
+                         h->pbits, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            e = cudaErrorInvalidValue;
+            goto fail_cuda;
+        }
+    }
     if (bad_host != 0) {
         status = BITLIN_EINVAL;
         goto fail;
@@ -251,7 +275,7 @@ fail:
 
 bitlin_status bitlin_set_path(bitlin_t h, int path)
 {
-    if (!h || path < BITLIN_PATH_AUTO || path > BITLIN_PATH_PREFILL) return BITLIN_EINVAL;
+    if (!h || path < BITLIN_PATH_AUTO || path > BITLIN_PATH_TC_EXACT) return BITLIN_EINVAL;
     h->path = path;
     return BITLIN_OK;
 }
@@ -276,8 +300,14 @@ bitlin_status bitlin_forward(bitlin_t h, const float* x, int M, float* y, bitlin
     if (h->sticky != BITLIN_OK) return h->sticky;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int path = h->path;
-    if (path == BITLIN_PATH_AUTO) path = (M >= kPrefillMinM) ? BITLIN_PATH_PREFILL : BITLIN_PATH_DECODE;
-    return path == BITLIN_PATH_PREFILL ? run_prefill(h, x, M, y, s) : run_decode(h, x, M, y, s);
+    if (path == BITLIN_PATH_AUTO)
+        path = M >= kPrefillMinM ? BITLIN_PATH_PREFILL : M >= 2 ? BITLIN_PATH_TC_EXACT : BITLIN_PATH_DECODE;
+    if (path == BITLIN_PATH_TC_EXACT && M >= kPrefillMinM) path = BITLIN_PATH_DECODE;  // exact tiles hold < 64 tokens
+    switch (path) {
+    case BITLIN_PATH_PREFILL: return run_tc(h, x, M, y, s, 0);
+    case BITLIN_PATH_TC_EXACT: return run_tc(h, x, M, y, s, 1);
+    default: return run_decode(h, x, M, y, s);
+    }
 }
 
 bitlin_status bitlin_forward_host(bitlin_t h, const float* x_host, int M, float* y_host,

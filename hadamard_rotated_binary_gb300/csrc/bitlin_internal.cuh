@@ -78,8 +78,10 @@ struct bitlin {
     unsigned* counters = nullptr;
     void* xt = nullptr;        // bf16 [M][K] rotated activations for the prefill path
     int xt_M = 0;
-    alignas(64) unsigned char tmap[128];  // TMA descriptor of xt (a CUtensorMap)
+    alignas(64) unsigned char tmap[128];       // TMA descriptor of xt (a CUtensorMap)
+    alignas(64) unsigned char tmap_bits[128];  // TMA descriptor of the tensor-path bits
     int tmap_M = 0;
+    int tmap_exact = -1;
     int* dev_error = nullptr;  // device error word [0]; [1] is create's sign check
     int* h_err = nullptr;      // pinned copy of the error word
     long long wait_budget_ns = 0;
@@ -99,6 +101,10 @@ cudaError_t bitlin_launch_repack_prefill(const uint32_t* bits, int N, int K, uin
 cudaError_t bitlin_launch_check_signs(const float* signs, int K, int* bad, cudaStream_t s);
 cudaError_t bitlin_launch_decode(const bitlin_impl::DecodeParams& p, int num_sms, cudaStream_t s);
 cudaError_t bitlin_launch_rotate_bf16(const float* x, const float* signs, int M, int K, int perm,
-                                      void* xt, cudaStream_t s);
-cudaError_t bitlin_launch_prefill(const bitlin_impl::PrefillParams& p, const void* tmap, int stall_test,
-                                  cudaStream_t s);
+                                      int digits, void* xt, cudaStream_t s);
+cudaError_t bitlin_launch_prefill(const bitlin_impl::PrefillParams& p, const void* tmap,
+                                  const void* tmap_bits, int stall_test, cudaStream_t s);
+cudaError_t bitlin_launch_tc_exact(const bitlin_impl::PrefillParams& p, const void* tmap,
+                                   const void* tmap_bits, int stall_test, cudaStream_t s);
+// Rows of B per tensor-core tile: 128 tokens (prefill) or 64/128/192/256 digit rows (exact).
+int bitlin_tc_tile_width(int M, int exact);

@@ -1,6 +1,9 @@
-// Stand-alone activation rotation for the tensor-core path: x f32 [M][K] ->
-// xt bf16 [M][K], xt = WHT1024(signs * P(x)) / 32 per block, rounded to
-// nearest-even bf16.  Pulse "ARCHITECTURE-SPEC", Hadamard-fold section
+// Stand-alone activation rotation for the tensor-core paths: x f32 [M][K] ->
+// xt = WHT1024(signs * P(x)) / 32 per block, stored as bf16 (round to nearest
+// even).  Prefill mode: one row per token, xt [M][K].  Exact mode: four rows
+// per token, [4M][K]: rows 4m, 4m+1, 4m+2 hold the digits hi = bf16(xt),
+// mid = bf16(xt - hi), lo = bf16(xt - hi - mid), whose sum is the f32 value,
+// and row 4m+3 is zero.  Pulse "ARCHITECTURE-SPEC", Hadamard-fold section
 // (order: optional tiled->grouped permutation, x * signs, normalized
 // Sylvester-Walsh transform in blocks of 1024 scaled by 1/32).
 //
@@ -24,7 +27,7 @@ __device__ __forceinline__ int perm_source(int k)
 
 __global__ void __launch_bounds__(256) bitlin_rotate_bf16(const float* __restrict__ x,
                                                           const float* __restrict__ signs, int M,
-                                                          int K, int perm,
+                                                          int K, int perm, int digits,
                                                           __nv_bfloat16* __restrict__ xt)
 {
     const int lane = threadIdx.x & 31;
@@ -60,20 +63,37 @@ __global__ void __launch_bounds__(256) bitlin_rotate_bf16(const float* __restric
             }
         }
     }
-    __nv_bfloat16* out = xt + (size_t)m * K + (size_t)b * 1024;
+    if (!digits) {
+        __nv_bfloat16* out = xt + (size_t)m * K + (size_t)b * 1024;
 #pragma unroll
-    for (int p = 0; p < 32; ++p) out[32 * p + lane] = __float2bfloat16_rn(v[p] * 0.03125f);
+        for (int p = 0; p < 32; ++p) out[32 * p + lane] = __float2bfloat16_rn(v[p] * 0.03125f);
+        return;
+    }
+    __nv_bfloat16* out = xt + (size_t)(4 * m) * K + (size_t)b * 1024;
+#pragma unroll
+    for (int p = 0; p < 32; ++p) {
+        const float t = v[p] * 0.03125f;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(t);
+        const float r1 = t - __bfloat162float(hi);  // exact
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const float r2 = r1 - __bfloat162float(mid);  // exact
+        const int k = 32 * p + lane;
+        out[k] = hi;
+        out[(size_t)K + k] = mid;
+        out[2 * (size_t)K + k] = __float2bfloat16_rn(r2);
+        out[3 * (size_t)K + k] = __float2bfloat16_rn(0.f);
+    }
 }
 
 }  // namespace
 
 cudaError_t bitlin_launch_rotate_bf16(const float* x, const float* signs, int M, int K, int perm,
-                                      void* xt, cudaStream_t s)
+                                      int digits, void* xt, cudaStream_t s)
 {
     const long long warps = (long long)M * (K / 1024);
     const int threads = 256;
     const long long blocks = (warps * 32 + threads - 1) / threads;
-    bitlin_rotate_bf16<<<(unsigned)blocks, threads, 0, s>>>(x, signs, M, K, perm,
+    bitlin_rotate_bf16<<<(unsigned)blocks, threads, 0, s>>>(x, signs, M, K, perm, digits,
                                                            static_cast<__nv_bfloat16*>(xt));
     return cudaGetLastError();
 }

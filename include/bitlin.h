@@ -25,11 +25,14 @@
  * sum then one multiply by the scale; station on the embedding row: bit k is
  * bit k&31 of word k>>5, scale index k>>7, IEEE binary16 scales).
  *
- * Paths: M < 64 runs the decode GEMV (f32 throughout; expected max relative
- * L2 error per token row <= 1e-5 against an exact evaluation).  M >= 64 runs
- * the tensor-core path: xt is rounded to bf16, the bits become +-1 bf16
- * operands of tcgen05 MMAs with f32 accumulation, and each group's partial
- * product is multiplied by its scale in f32 (expected error <= 1e-2).
+ * Paths: M = 1 runs the decode GEMV (f32 throughout; expected max relative L2
+ * error per token row <= 1e-5 against an exact evaluation).  2 <= M < 64 runs
+ * the tensor-core path with xt split exactly into three bf16 digits, so the
+ * +-1 x digit products and f32 accumulation give f32-level results (<= 1e-5).
+ * M >= 64 runs the tensor-core path with xt rounded to bf16 (<= 1e-2).  In
+ * both tensor-core paths the bits become +-1 bf16 operands of tcgen05 MMAs
+ * with f32 accumulation, and each group's partial product is multiplied by
+ * its scale in f32.
  *
  * Errors: every function returns a bitlin_status and never aborts or prints.
  * Threads: a handle may be used from one host thread / one stream at a time.
@@ -65,9 +68,11 @@ typedef enum {
  * (Pulse "ARCHITECTURE-SPEC", ssm_out permutation paragraph.) */
 #define BITLIN_PERM_SSM_TILED_TO_GROUPED 1
 
-#define BITLIN_PATH_AUTO 0    /* M < 64 -> decode, M >= 64 -> tensor-core prefill */
-#define BITLIN_PATH_DECODE 1  /* force the f32 decode GEMV for every M */
-#define BITLIN_PATH_PREFILL 2 /* force the tcgen05 bf16 path for every M */
+#define BITLIN_PATH_AUTO 0     /* M = 1 -> decode GEMV, 2 <= M < 64 -> exact tensor path, M >= 64 -> prefill */
+#define BITLIN_PATH_DECODE 1   /* force the f32 decode GEMV (shared-memory tables) for every M */
+#define BITLIN_PATH_PREFILL 2  /* force the tcgen05 path with bf16 activations for every M */
+#define BITLIN_PATH_TC_EXACT 3 /* force the tcgen05 path with activations split into three bf16
+                                  digits (f32-level results) for M < 64; decode GEMV above */
 
 /*
  * Create a handle for one N x K folded 1-bit matrix on the current device.

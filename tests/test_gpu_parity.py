@@ -234,6 +234,36 @@ def test_forward_host_buffers(hrb):
     assert max_rel_l2(y.astype(np.float64), ref) <= DECODE_TOL
 
 
+# ------------------------------------------------------------------ exact tensor path (2 <= M < 64)
+
+@pytest.mark.parametrize("M,N,K,perm", [(2, 256, 1024, 0), (16, 1000, 2048, 0), (17, 384, 6144, 1),
+                                        (40, 300, 3072, 0), (63, 129, 1024, 0)])
+def test_tc_exact_path_every_tile_width(hrb, M, N, K, perm):
+    """Activations split into three bf16 digits: f32-level results at every tile width (64..256)."""
+    seed = 23 + M + N + K
+    bits = synth.random_bits(seed, N, K)
+    scales = synth.random_scales(seed, N, K, 0.005, 0.03)
+    signs = synth.random_signs(seed, K)
+    x = synth.random_x(seed, M, K)
+    layer = make_layer(hrb, bits, scales, signs, perm)
+    y = run(layer, x, path=hrb.PATH_TC_EXACT)
+    ref = oracle.forward(bits, scales, signs, perm, x)
+    assert max_rel_l2(y, ref) <= DECODE_TOL
+    y_dec = run(layer, x, path=hrb.PATH_DECODE)
+    assert max_rel_l2(y_dec, ref) <= DECODE_TOL
+
+
+def test_auto_path_choice(hrb):
+    """M = 1 -> table GEMV, 2..63 -> exact tensor path, >= 64 -> bf16 tensor path; all in tolerance."""
+    w, bits, scales, signs, x = inputs("ffn_gate", 70)
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    rows = synth.sample_rows(w.seed, w.N, 256)
+    ref = oracle.forward(bits, scales, signs, 0, x, rows)
+    for m, tol in ((1, DECODE_TOL), (2, DECODE_TOL), (63, DECODE_TOL), (64, PREFILL_TOL), (70, PREFILL_TOL)):
+        y = run(layer, np.ascontiguousarray(x[:m]))
+        assert max_rel_l2(y[:, rows], ref[:m]) <= tol, m
+
+
 # ------------------------------------------------------------------ errors
 
 def test_signs_must_be_plus_minus_one(hrb):
