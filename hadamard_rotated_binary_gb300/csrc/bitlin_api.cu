@@ -91,11 +91,13 @@ bitlin_status ensure_xt(bitlin_t h, int M, int exact)
     if (h->tmap_M != M || h->tmap_exact != exact) {
         PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
         if (!enc) return from_cuda(h, cudaErrorNotSupported);
-        cuuint64_t dims[2] = {(cuuint64_t)h->K, (cuuint64_t)rows};
-        cuuint64_t strides[1] = {(cuuint64_t)h->K * 2};
-        cuuint32_t box[2] = {64, (cuuint32_t)bitlin_tc_tile_width(M, exact)};
-        cuuint32_t estr[2] = {1, 1};
-        CUresult r = enc(reinterpret_cast<CUtensorMap*>(h->tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+        // Viewed as [K/64][rows][64]: one box {64, tile width, 2} is a K-group's
+        // two 128-byte-swizzled halves, stacked, in a single copy.
+        cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(h->K / 64)};
+        cuuint64_t strides[2] = {(cuuint64_t)h->K * 2, 128};
+        cuuint32_t box[3] = {64, (cuuint32_t)bitlin_tc_tile_width(M, exact), 2};
+        cuuint32_t estr[3] = {1, 1, 1};
+        CUresult r = enc(reinterpret_cast<CUtensorMap*>(h->tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                          h->xt, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -302,7 +304,6 @@ bitlin_status bitlin_forward(bitlin_t h, const float* x, int M, float* y, bitlin
     int path = h->path;
     if (path == BITLIN_PATH_AUTO)
         path = M >= kPrefillMinM ? BITLIN_PATH_PREFILL : M >= 2 ? BITLIN_PATH_TC_EXACT : BITLIN_PATH_DECODE;
-    if (path == BITLIN_PATH_TC_EXACT && M >= kPrefillMinM) path = BITLIN_PATH_DECODE;  // exact tiles hold < 64 tokens
     switch (path) {
     case BITLIN_PATH_PREFILL: return run_tc(h, x, M, y, s, 0);
     case BITLIN_PATH_TC_EXACT: return run_tc(h, x, M, y, s, 1);

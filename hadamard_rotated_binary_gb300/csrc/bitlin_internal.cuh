@@ -26,7 +26,6 @@ constexpr int kTicketStride = 32;     // one split-K ticket per 128-byte line
 // ---- prefill layout ------------------------------------------------------
 constexpr int kPrefillRows = 128;     // weight rows per CTA (UMMA M)
 constexpr int kPrefillTokens = 128;   // tokens per CTA (UMMA N)
-constexpr int kPrefillStages = 3;
 constexpr int kPrefillMinM = 64;      // auto path switch
 
 // Device-side error word values (bitlin_t::dev_error).

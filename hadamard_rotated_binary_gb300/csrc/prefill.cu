@@ -13,30 +13,33 @@
 //    the three bf16 digits hi, mid, lo of xt (hi = bf16(xt), mid =
 //    bf16(xt - hi), lo = bf16(xt - hi - mid): together the f32 value) and row
 //    4m+3 = 0.  Products with +-1 are exact, so summing the three digit
-//    columns of D gives f32-level results.  One tile holds every token.
+//    columns of D gives f32-level results.  A tile of BN rows holds BN/4
+//    whole tokens.
 //
 // CTA tile: 128 weight rows (UMMA M = 128, one TMEM lane per row) x BN columns
-// of B (UMMA N = BN).  Per 128-wide K-group g:
-//   * warp 8, lane 0 TMA-loads the B tile [BN rows][128 K] as two
-//     128-byte-swizzled boxes of 64 columns; lane 1 TMA-loads the group's
-//     bits [128 rows][4 words] (2 KB) into a separate ring that runs up to 8
-//     groups ahead, so the expansion never waits for the B tile;
-//   * warps 10-13 (one thread per weight row) expand that row's 128 bits of
-//     the group into +-1 bf16 directly in the same swizzled K-major layout (TMA
-//     cannot expand bits).  The repack stores even weights in the low
-//     half-word and odd weights in the high half-word, so each bf16x2 pair is
-//     one shift and one XOR-mask;
-//   * warp 9 (one lane) issues 8 MMAs of K = 16 into TMEM accumulator
-//     buffer g % 2 (overwriting it at the first), then commits to the stage's
-//     "empty" barrier and the buffer's "full" barrier;
+// of B (UMMA N = BN).  The +-1 operand A lives in tensor memory, so shared
+// memory holds only B tiles (deep enough to cover the ~1 us a copy from L2
+// takes when every SM streams) and the packed bits.  Per 128-wide K-group g:
+//   * warp 8 TMA-loads the B tile [BN rows][128 K] (one 3-d box: two
+//     128-byte-swizzled 64-column halves); warp 14 TMA-loads the group's bits
+//     [128 rows][4 words] (2 KB) into a ring that runs up to 8 groups ahead;
+//   * warps 10-13 (one thread per weight row = TMEM lane) turn that row's 128
+//     bits into 64 columns of bf16 pairs (+-1) and store them to the group's
+//     A stage in tensor memory (tcgen05.st).  The repack stores even weights
+//     in the low half-word and odd weights in the high half-word, so each
+//     bf16x2 column is one shift and one XOR-mask;
+//   * warp 9 waits for A, B and a free accumulator buffer (one round trip:
+//     the three barriers are tested together); one elected lane issues 8
+//     MMAs of K = 16 (A from tensor memory, B from shared memory) into buffer
+//     g % 2, then commits to the group's "done" barrier (frees the A and B
+//     stages) and the buffer's "full" barrier;
 //   * warps 0-7 read the buffer back (tcgen05.ld), hand it back to the MMA
 //     warp, and accumulate scale[n][g] * D into f32 registers - the per-group
 //     scale promotion.  Warp w serves TMEM lanes 32*(w%4).. and the columns
 //     BN/2*(w/4) .. BN/2*(w/4) + BN/2 - 1.  Scales are requested 4 groups ahead.
-// Shared-memory stages keep the producers ahead of the MMAs, two TMEM buffers
-// keep the MMAs one group ahead of the epilogue.  Every wait is bounded in
-// time; on expiry the kernel stops its loops, drains its own copies and
-// MMAs, frees TMEM and records a timeout in the handle's error word.
+// Every wait is bounded in time; on expiry the kernel stops its loops, drains
+// its own copies and MMAs, frees TMEM and records a timeout in the handle's
+// error word.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -48,60 +51,76 @@ namespace {
 
 using namespace bitlin_impl;
 
-constexpr int kThreads = 448;       // 14 warps
+constexpr int kThreads = 480;       // 15 warps
 constexpr int kEpiWarps = 8;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kExpWarp0 = 10;
-constexpr int kABytes = 32768;      // A tile: 128 rows x 128 bf16
+constexpr int kExpWarp0 = 10;       // warps 10..13
+constexpr int kBitsWarp = 14;
 constexpr int kBitsBytes = 2048;    // one group's bits: 128 rows x 4 words
 constexpr int kBitsStages = 8;      // bits run this many groups ahead of the expansion
+constexpr int kACols = 64;          // one A stage: 128 lanes x 64 columns (128 bf16 per row)
+constexpr int kTmemCols = 512;      // the whole tensor memory (one CTA per SM)
 
-template <int STAGES>
+template <int BN>
+struct Cfg {
+    static constexpr int kBBytes = BN * 256;  // B tile: BN rows x 128 bf16
+    static constexpr int kSmemBudget = 200 * 1024 - kBitsStages * kBitsBytes;
+    static constexpr int kStagesB = kSmemBudget / kBBytes > 8 ? 8 : kSmemBudget / kBBytes;
+    static constexpr int kStagesA = (kTmemCols - 2 * BN) / kACols > 6 ? 6 : (kTmemCols - 2 * BN) / kACols;
+    static constexpr int kRing = kStagesA > kStagesB ? kStagesA : kStagesB;  // "done" barriers
+    static_assert(kStagesB >= 3 && kStagesA >= 2, "pipeline depth");
+};
+
+template <int BN>
 struct __align__(8) Barriers {
-    uint64_t fullA[STAGES];
-    uint64_t fullB[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t fullB[Cfg<BN>::kStagesB];  // B tile landed (1 arrival + bytes)
+    uint64_t fullA[Cfg<BN>::kStagesA];  // A stage written (128 arrivals: one thread per row)
+    uint64_t done[Cfg<BN>::kRing];      // the MMAs of group g (index g % kRing) completed
     uint64_t fullBits[kBitsStages];
     uint64_t emptyBits[kBitsStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
-    uint64_t never;     // no one arrives here: used by the stall test hook
+    uint64_t never;  // no one arrives here: used by the stall test hook
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
 
 template <int BN>
-struct Cfg {
-    static constexpr int kBBytes = BN * 256;  // B tile: BN rows x 128 bf16
-    static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kBudget = 208 * 1024 - kBitsStages * kBitsBytes;
-    static constexpr int kStages = kStageBytes * 4 <= kBudget ? 4 : kStageBytes * 3 <= kBudget ? 3 : 2;
-    static constexpr int kTmemCols = 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
-    static constexpr int kSmem =
-        kStages * kStageBytes + kBitsStages * kBitsBytes + (int)sizeof(Barriers<kStages>) + 1024;
-};
+constexpr int smem_bytes()
+{
+    return Cfg<BN>::kStagesB * Cfg<BN>::kBBytes + kBitsStages * kBitsBytes + (int)sizeof(Barriers<BN>) + 1024;
+}
+
+// Wait until the MMAs of group h have completed (h >= 0), through the "done"
+// ring: phase h / R of barrier h % R.  A waiter never runs more than one phase
+// ahead: it has already seen group h - 1 complete.
+template <int R>
+__device__ __forceinline__ bool wait_done(uint64_t* done, int h, volatile int* abort, long long budget)
+{
+    return ptx::mbar_wait_bounded(&done[h % R], (uint32_t)(h / R) & 1u, abort, budget);
+}
 
 template <int BN, bool EXACT>
 __global__ void __launch_bounds__(kThreads, 1)
     bitlin_tc_gemm(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_bits,
                    const PrefillParams p, int stall_test)
 {
-    constexpr int STAGES = Cfg<BN>::kStages;
-    constexpr int kBBytes = Cfg<BN>::kBBytes;
+    using C = Cfg<BN>;
+    constexpr int SB = C::kStagesB, SA = C::kStagesA, R = C::kRing;
+    constexpr int kBBytes = C::kBBytes;
     constexpr int kHalf = BN / 2;                    // columns per epilogue warp
     constexpr int kChunks = kHalf / 32;              // tcgen05.ld x32 loads per group
     constexpr int kAcc = EXACT ? kHalf / 4 : kHalf;  // accumulators per epilogue thread
-    static_assert(BN % 64 == 0 && BN <= 256, "tile width");
+    static_assert(BN % 64 == 0 && BN <= 128, "tile width");
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    unsigned char* tileA = smem;                         // [stage][32 KB]
-    unsigned char* tileB = smem + STAGES * kABytes;      // [stage][BN * 256 B]
-    unsigned char* tileBits = tileB + STAGES * kBBytes;  // [bits stage][2 KB]: [row][4 words]
-    auto* bar = reinterpret_cast<Barriers<STAGES>*>(tileBits + kBitsStages * kBitsBytes);
+    unsigned char* tileB = smem;                         // [stage][BN * 256 B]
+    unsigned char* tileBits = tileB + SB * kBBytes;      // [bits stage][2 KB]: [row][4 words]
+    auto* bar = reinterpret_cast<Barriers<BN>*>(tileBits + kBitsStages * kBitsBytes);
     volatile int* abort = &bar->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -111,11 +130,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long budget = p.wait_budget_ns;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(&bar->fullA[s], 128);
-            ptx::mbar_init(&bar->fullB[s], 1);
-            ptx::mbar_init(&bar->empty[s], 1);
-        }
+        for (int s = 0; s < SB; ++s) ptx::mbar_init(&bar->fullB[s], 1);
+        for (int s = 0; s < SA; ++s) ptx::mbar_init(&bar->fullA[s], 128);
+        for (int s = 0; s < R; ++s) ptx::mbar_init(&bar->done[s], 1);
         for (int s = 0; s < kBitsStages; ++s) {
             ptx::mbar_init(&bar->fullBits[s], 1);
             ptx::mbar_init(&bar->emptyBits[s], 128);
@@ -131,42 +148,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_proxy_async_smem();
     }
     if (warp == kMmaWarp) {
-        ptx::tmem_alloc(&bar->tmem_base, Cfg<BN>::kTmemCols);
+        ptx::tmem_alloc(&bar->tmem_base, kTmemCols);
         ptx::tmem_relinquish();
     }
-    if (warp == kTmaWarp && lane == 0) {
-        ptx::prefetch_tmap(&tmap_b);
-        ptx::prefetch_tmap(&tmap_bits);
-    }
+    if (warp == kTmaWarp && lane == 0) ptx::prefetch_tmap(&tmap_b);
+    if (warp == kBitsWarp && lane == 0) ptx::prefetch_tmap(&tmap_bits);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = bar->tmem_base;
+    const uint32_t tmemA = tmem + 2 * BN;  // A stages follow the two accumulator buffers
 
     if (warp == kTmaWarp) {
         if (lane == 0) {
-            // B tiles, gated by the stage's "empty" barrier (the MMAs of the
-            // group STAGES back have completed).
+            // B tiles; stage g % SB is free once the MMAs of group g - SB completed.
             int issued = 0;
             for (int g = 0; g < G; ++g) {
-                const int st = g % STAGES;
-                const uint32_t ph = (uint32_t)(g / STAGES) & 1u;
-                if (!ptx::mbar_wait_bounded(&bar->empty[st], ph ^ 1u, abort, budget)) break;
+                const int st = g % SB;
+                if (g >= SB && !wait_done<R>(bar->done, g - SB, abort, budget)) break;
                 ptx::mbar_arrive_expect_tx(&bar->fullB[st], kBBytes);
-                unsigned char* dst = tileB + st * kBBytes;
-                ptx::tma_load_2d(dst, &tmap_b, g * 128, b0, &bar->fullB[st]);
-                ptx::tma_load_2d(dst + kBBytes / 2, &tmap_b, g * 128 + 64, b0, &bar->fullB[st]);
+                ptx::tma_load_3d(tileB + st * kBBytes, &tmap_b, 0, b0, 2 * g, &bar->fullB[st]);
                 issued = g + 1;
             }
             // Every copy this lane issued must land before the CTA may exit.
-            for (int g = (issued > STAGES ? issued - STAGES : 0); g < issued; ++g) {
-                const int st = g % STAGES;
-                const uint32_t ph = (uint32_t)(g / STAGES) & 1u;
+            for (int g = (issued > SB ? issued - SB : 0); g < issued; ++g) {
                 volatile int no_abort = 0;
-                ptx::mbar_wait_bounded(&bar->fullB[st], ph, &no_abort, budget);
+                ptx::mbar_wait_bounded(&bar->fullB[g % SB], (uint32_t)(g / SB) & 1u, &no_abort, budget);
             }
-        } else if (lane == 1) {
-            // Bits, up to kBitsStages groups ahead of the expansion.
+        }
+    } else if (warp == kBitsWarp) {
+        // Bits, up to kBitsStages groups ahead of the expansion (a warp of its
+        // own: two producers in one warp would take turns).
+        if (lane == 0) {
             int issued = 0;
             for (int g = 0; g < G; ++g) {
                 const int sb = g % kBitsStages;
@@ -184,73 +197,74 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == kMmaWarp) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(kPrefillRows, BN);
-            int issued = 0;
-            for (int g = 0; g < G; ++g) {
-                const int st = g % STAGES;
-                const uint32_t ph = (uint32_t)(g / STAGES) & 1u;
-                const int buf = g & 1;
-                const uint32_t tph = (uint32_t)(g >> 1) & 1u;
-                if (!ptx::mbar_wait_bounded(&bar->fullA[st], ph, abort, budget)) break;
-                if (!ptx::mbar_wait_bounded(&bar->fullB[st], ph, abort, budget)) break;
-                if (!ptx::mbar_wait_bounded(&bar->tempty[buf], tph ^ 1u, abort, budget)) break;
-                ptx::tc_fence_after();
-                const uint32_t a0 = ptx::smem_u32(tileA + st * kABytes);
-                const uint32_t bb = ptx::smem_u32(tileB + st * kBBytes);
+        // The whole warp runs the loop and checks the barriers; one elected lane
+        // issues.  The tensor pipe queues only a few MMAs, so the checks before
+        // a group take one shared-memory round trip.
+        constexpr uint32_t idesc = ptx::idesc_bf16_f32(kPrefillRows, BN);
+        const uint64_t descB = ptx::smem_desc_sw128(ptx::smem_u32(tileB));
+        int issued = 0;
+        for (int g = 0; g < G; ++g) {
+            const int sb = g % SB, sa = g % SA, buf = g & 1;
+            if (!ptx::mbar_wait3_bounded(&bar->fullB[sb], (uint32_t)(g / SB) & 1u, &bar->fullA[sa],
+                                         (uint32_t)(g / SA) & 1u, &bar->tempty[buf], ((uint32_t)(g >> 1) & 1u) ^ 1u,
+                                         abort, budget))
+                break;
+            ptx::tc_fence_after();
+            if (ptx::elect_one()) {
                 const uint32_t d = tmem + (uint32_t)(buf * BN);
+                const uint32_t a = tmemA + (uint32_t)(sa * kACols);
+                // Descriptor start addresses advance in 16-byte units.
+                const uint64_t db = descB + (uint64_t)((sb * kBBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t offa = (uint32_t)((kk >> 2) * (kABytes / 2) + (kk & 3) * 32);
-                    const uint32_t offb = (uint32_t)((kk >> 2) * (kBBytes / 2) + (kk & 3) * 32);
-                    ptx::mma_bf16(d, ptx::smem_desc_sw128(a0 + offa), ptx::smem_desc_sw128(bb + offb),
-                                  idesc, kk > 0 ? 1u : 0u);
+                    const uint32_t offb = (uint32_t)((kk >> 2) * (kBBytes / 2) + (kk & 3) * 32) >> 4;
+                    ptx::mma_bf16_ts(d, a + 8 * kk, db + offb, idesc, kk > 0 ? 1u : 0u);
                 }
-                ptx::mma_commit(&bar->empty[st]);
+                ptx::mma_commit(&bar->done[g % R]);
                 ptx::mma_commit(&bar->tfull[buf]);
-                issued = g + 1;
             }
-            // Wait for every MMA issued here before TMEM is released.
-            if (issued > 0) {
-                ptx::mma_commit(&bar->drain);
-                volatile int no_abort = 0;
-                ptx::mbar_wait_bounded(&bar->drain, 0u, &no_abort, budget);
-            }
+            __syncwarp();
+            issued = g + 1;
         }
-    } else if (warp >= kExpWarp0) {
-        const int r = (warp - kExpWarp0) * 32 + lane;  // row within the tile
+        // Wait for every MMA issued here before TMEM is released.
+        if (issued > 0) {
+            if (ptx::elect_one()) ptx::mma_commit(&bar->drain);
+            __syncwarp();
+            volatile int no_abort = 0;
+            ptx::mbar_wait_bounded(&bar->drain, 0u, &no_abort, budget);
+        }
+    } else if (warp >= kExpWarp0 && warp < kExpWarp0 + 4) {
+        // A warp may only reach TMEM lanes 32*(warp%4) .. +31: row = that lane.
+        const int r = 32 * (warp & 3) + lane;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         for (int g = 0; g < G; ++g) {
-            const int st = g % STAGES;
-            const uint32_t ph = (uint32_t)(g / STAGES) & 1u;
+            const int sa = g % SA;
             const int sb = g % kBitsStages;
-            const uint32_t phb = (uint32_t)(g / kBitsStages) & 1u;
             // The group's bits (prefetched up to kBitsStages groups ahead), then a
-            // free A buffer: the MMAs of the group STAGES back have completed.
-            if (!ptx::mbar_wait_bounded(&bar->fullBits[sb], phb, abort, budget)) break;
+            // free A stage: the MMAs of group g - SA have completed.
+            if (!ptx::mbar_wait_bounded(&bar->fullBits[sb], (uint32_t)(g / kBitsStages) & 1u, abort, budget)) break;
             const uint4 wq = *reinterpret_cast<const uint4*>(tileBits + sb * kBitsBytes + r * 16);
             ptx::mbar_arrive(&bar->emptyBits[sb]);
-            if (!ptx::mbar_wait_bounded(&bar->empty[st], ph ^ 1u, abort, budget)) break;
-            unsigned char* dst = tileA + st * kABytes + r * 128;
+            if (g >= SA && !wait_done<R>(bar->done, g - SA, abort, budget)) break;
+            ptx::tc_fence_after();
             const uint32_t words[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                // chunk c = weights 8c .. 8c+7 of the group = pairs 4(c&3) .. 4(c&3)+3 of word c>>2
-                const uint32_t W = words[c >> 2];
-                uint32_t v[4];
+            for (int h = 0; h < 2; ++h) {
+                // columns 32h .. 32h+31 = words 2h, 2h+1; column 16j + i holds weights
+                // 32j + 2i (low half) and 32j + 2i + 1 (high half)
+                uint32_t v[32];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int i = 4 * (c & 3) + q;
-                    v[q] = 0xBF80BF80u ^ ((W << (15 - i)) & 0x80008000u);
+                for (int c = 0; c < 32; ++c) {
+                    const uint32_t W = words[2 * h + (c >> 4)];
+                    v[c] = 0xBF80BF80u ^ ((W << (15 - (c & 15))) & 0x80008000u);
                 }
-                const int atom = c >> 3, cc = c & 7;
-                *reinterpret_cast<uint4*>(dst + atom * (kABytes / 2) + ((cc ^ (r & 7)) << 4)) =
-                    make_uint4(v[0], v[1], v[2], v[3]);
+                ptx::tmem_st32(tmemA + lane_base + (uint32_t)(sa * kACols + 32 * h), v);
             }
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(&bar->fullA[st]);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar->fullA[sa]);
         }
-    } else {
-        // Epilogue warps 0..7.
+    } else if (warp < kEpiWarps) {
         const int q = warp & 3, half = warp >> 2;
         const int r = 32 * q + lane;
         const int n = n0 + r;
@@ -303,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && valid) {
 #pragma unroll
             for (int j = 0; j < kAcc; ++j) {
-                const int m = EXACT ? (half * (kHalf / 4) + j) : (b0 + half * kHalf + j);
+                const int m = EXACT ? (b0 + half * kHalf) / 4 + j : b0 + half * kHalf + j;
                 if (m < p.M) p.y[(size_t)m * p.N + n] = acc[j];
             }
         }
@@ -313,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == kMmaWarp) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, Cfg<BN>::kTmemCols);
+        ptx::tmem_dealloc(tmem, kTmemCols);
     }
     if (threadIdx.x == 0 && bar->abort) atomicExch(p.dev_error, kDevErrTimeout);
 }
@@ -325,13 +339,13 @@ cudaError_t launch(const PrefillParams& p, const void* tmap, const void* tmap_bi
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(bitlin_tc_gemm<BN, EXACT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::kSmem);
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<BN>());
         if (e != cudaSuccess) return e;
         configured = true;
     }
     const int rows_b = EXACT ? 4 * p.M : p.M;
     dim3 grid((p.N + kPrefillRows - 1) / kPrefillRows, (rows_b + BN - 1) / BN);
-    bitlin_tc_gemm<BN, EXACT><<<grid, kThreads, Cfg<BN>::kSmem, s>>>(
+    bitlin_tc_gemm<BN, EXACT><<<grid, kThreads, smem_bytes<BN>(), s>>>(
         *static_cast<const CUtensorMap*>(tmap), *static_cast<const CUtensorMap*>(tmap_bits), p, stall_test);
     return cudaGetLastError();
 }
@@ -341,8 +355,7 @@ cudaError_t launch(const PrefillParams& p, const void* tmap, const void* tmap_bi
 int bitlin_tc_tile_width(int M, int exact)
 {
     if (!exact) return kPrefillTokens;
-    const int rows = 4 * M;
-    return rows <= 64 ? 64 : rows <= 128 ? 128 : rows <= 192 ? 192 : 256;
+    return 4 * M <= 64 ? 64 : 128;
 }
 
 cudaError_t bitlin_launch_prefill(const PrefillParams& p, const void* tmap, const void* tmap_bits,
@@ -354,10 +367,6 @@ cudaError_t bitlin_launch_prefill(const PrefillParams& p, const void* tmap, cons
 cudaError_t bitlin_launch_tc_exact(const PrefillParams& p, const void* tmap, const void* tmap_bits,
                                    int stall_test, cudaStream_t s)
 {
-    switch (bitlin_tc_tile_width(p.M, 1)) {
-    case 64: return launch<64, true>(p, tmap, tmap_bits, stall_test, s);
-    case 128: return launch<128, true>(p, tmap, tmap_bits, stall_test, s);
-    case 192: return launch<192, true>(p, tmap, tmap_bits, stall_test, s);
-    default: return launch<256, true>(p, tmap, tmap_bits, stall_test, s);
-    }
+    if (bitlin_tc_tile_width(p.M, 1) == 64) return launch<64, true>(p, tmap, tmap_bits, stall_test, s);
+    return launch<128, true>(p, tmap, tmap_bits, stall_test, s);
 }

@@ -48,6 +48,8 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
         : "memory");
 }
 
+// Potentially blocking check: returns once the phase with the given parity
+// has completed or a hardware-chosen time limit has passed.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 {
     uint32_t ok;
@@ -60,8 +62,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
-// Non-blocking check of the phase with the given parity (a few ns, whereas
-// try_wait costs tens of ns even on a completed phase).
+// Non-blocking check of whether the phase with the given parity has completed.
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
 {
     uint32_t ok;
@@ -74,9 +75,33 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// Three checks in one go: the shared-memory lookups are in flight together
+// instead of one after the other.
+__device__ __forceinline__ bool mbar_test_wait3(uint64_t* bar0, uint32_t parity0, uint64_t* bar1,
+                                                uint32_t parity1, uint64_t* bar2, uint32_t parity2)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p0, p1, p2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p0, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p1, [%3], %4;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p2, [%5], %6;\n\t"
+        "and.pred p0, p0, p1;\n\t"
+        "and.pred p0, p0, p2;\n\t"
+        "selp.u32 %0, 1, 0, p0;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar0)), "r"(parity0), "r"(smem_u32(bar1)), "r"(parity1), "r"(smem_u32(bar2)),
+          "r"(parity2)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up (returns
 // false) when *abort is set by another thread or when budget_ns of wall time
-// pass, in which case it sets *abort itself.
+// pass, in which case it sets *abort itself.  A completed phase is seen by
+// test_wait (a few ns); otherwise try_wait lets the thread sleep until the
+// phase completes or a hardware time limit passes, which keeps the waiting
+// warps off the issue slots that the working warps need.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, long long budget_ns)
 {
@@ -95,6 +120,28 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// All three phases, bounded as mbar_wait_bounded; the common case (all
+// already complete) costs one round trip to shared memory.
+__device__ __forceinline__ bool mbar_wait3_bounded(uint64_t* bar0, uint32_t parity0, uint64_t* bar1,
+                                                   uint32_t parity1, uint64_t* bar2, uint32_t parity2,
+                                                   volatile int* abort, long long budget_ns)
+{
+    if (mbar_test_wait3(bar0, parity0, bar1, parity1, bar2, parity2)) return true;
+    return mbar_wait_bounded(bar0, parity0, abort, budget_ns) && mbar_wait_bounded(bar1, parity1, abort, budget_ns) &&
+           mbar_wait_bounded(bar2, parity2, abort, budget_ns);
+}
+
+// One lane of a converged warp (elect.sync): true on exactly one lane.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\telect.sync r|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ---- fences ----------------------------------------------------------------
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor core / TMA reads).
@@ -111,6 +158,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int c0,
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Box at (c0, c1, c2) of a 3-d tensor map.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int c0, int c1, int c2,
+                                            uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -153,6 +211,18 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16: A is read from tensor memory
+// (row i of A in lane i, two bf16 per 32-bit column, lower K in the low half).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on bar when every tcgen05.mma issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t* bar)
 {
@@ -180,6 +250,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// Store 32 consecutive 32-bit columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 

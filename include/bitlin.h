@@ -72,7 +72,7 @@ typedef enum {
 #define BITLIN_PATH_DECODE 1   /* force the f32 decode GEMV (shared-memory tables) for every M */
 #define BITLIN_PATH_PREFILL 2  /* force the tcgen05 path with bf16 activations for every M */
 #define BITLIN_PATH_TC_EXACT 3 /* force the tcgen05 path with activations split into three bf16
-                                  digits (f32-level results) for M < 64; decode GEMV above */
+                                  digits (f32-level results) for every M */
 
 /*
  * Create a handle for one N x K folded 1-bit matrix on the current device.

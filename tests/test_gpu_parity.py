@@ -237,9 +237,10 @@ def test_forward_host_buffers(hrb):
 # ------------------------------------------------------------------ exact tensor path (2 <= M < 64)
 
 @pytest.mark.parametrize("M,N,K,perm", [(2, 256, 1024, 0), (16, 1000, 2048, 0), (17, 384, 6144, 1),
-                                        (40, 300, 3072, 0), (63, 129, 1024, 0)])
+                                        (40, 300, 3072, 0), (63, 129, 1024, 0), (100, 200, 1024, 0)])
 def test_tc_exact_path_every_tile_width(hrb, M, N, K, perm):
-    """Activations split into three bf16 digits: f32-level results at every tile width (64..256)."""
+    """Activations split into three bf16 digits: f32-level results at both tile widths (64, 128) and
+    with the tokens spread over several tiles (M = 40, 63, 100)."""
     seed = 23 + M + N + K
     bits = synth.random_bits(seed, N, K)
     scales = synth.random_scales(seed, N, K, 0.005, 0.03)
