@@ -142,6 +142,17 @@ def traffic_record(kernel: str, workload: str):
     return entry["bytes_per_launch"] if digest == entry["sha256"] else None
 
 
+def max_over_ranks(v: float, pg, device) -> float:
+    """The largest of every rank's v (the slowest rank's time), on every rank; v itself at N = 1."""
+    if pg is None:
+        return v
+    import torch
+
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
 def path_of(w: synth.Workload) -> str:
     """Kernel that does the bulk of one call: the decode GEMV (M = 1) or the tcgen05 GEMM."""
     return "bitlin_decode_gemv" if w.M == 1 else "bitlin_tc_gemm"
@@ -326,11 +337,7 @@ def main():
     if pg:
         pg.barrier()
     clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1)
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
     assert layers[0].get_error() == 0
 
     # End to end through the host-buffer entry point (pinned host memory).
@@ -344,11 +351,7 @@ def main():
     t0 = time.perf_counter()
     for i in range(e2e_steps):
         layers[i % R].forward_host(xh, yh, stream=stream)
-    e2e_s = time.perf_counter() - t0
-    if pg:
-        t = torch.tensor([e2e_s], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, pg, dev)
 
     if rank != 0:
         if pg:
