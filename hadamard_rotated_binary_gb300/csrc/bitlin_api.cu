@@ -126,6 +126,9 @@ bitlin_status run_decode(bitlin_t h, const float* x, int M, float* y, cudaStream
     p.S = h->S;
     p.T = h->T;
     p.perm = h->perm;
+    p.ctas_per_slice = 0;
+    p.cluster = 0;
+    p.allow_cluster = 1;
     return from_cuda(h, bitlin_launch_decode(p, h->num_sms, s));
 }
 

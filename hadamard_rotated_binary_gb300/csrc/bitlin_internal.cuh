@@ -41,6 +41,8 @@ struct DecodeParams {
     unsigned* counters;     // [T * kTicketStride] split-K tickets, zero between calls
     int M, N, K, S, T, perm;
     int ctas_per_slice;     // set by the launcher
+    int cluster;            // set by the launcher: 1 = split-K summed across a thread-block cluster
+    int allow_cluster;      // set by the caller: 0 keeps the split-K in the global scratch
 };
 
 struct PrefillParams {

@@ -8,7 +8,7 @@
 //
 // How (GB300 design):
 //  * Work unit = (slice s of 512 weights along K) x (tile t of 32 rows).  A CTA
-//    (8 warps, one per SM) owns one slice and a contiguous range of tiles.
+//    (16 warps, one per SM) owns one slice and a contiguous range of tiles.
 //    Split-K partial sums land in a scratch array; at the end each CTA takes
 //    one ticket per tile in parallel, and the CTA that draws the last ticket
 //    of a tile sums its S partials in fixed order s = 0..S-1 (deterministic)
@@ -33,16 +33,17 @@
 //    builds the whole shared-memory offset from the byte and a per-lane
 //    register), one LDS and one FADD.  Every 4 words (one 128-group) the
 //    group sum is multiplied by its fp16 scale with one FFMA.
-//  * Weights stream straight from HBM into registers with 16-byte coalesced
-//    loads through a ring of 4 tiles per warp: the first 4 tiles are requested
-//    before the prologue (so DRAM latency overlaps the transform and the table
-//    build) and each consumed tile is replaced by the warp's next one.
-//  * At most 128 registers and 70 KB of shared memory per CTA, so a second
-//    CTA fits on each SM: the next call's CTAs become resident while this
-//    call finishes and start streaming their weights.
-//  * Programmatic dependent launch: the kernel lets its successor launch at
-//    once and itself waits (griddepcontrol.wait) only before it reads x or
-//    writes any output; weight prefetch precedes the wait.
+//  * Weights stream from HBM into registers with 16-byte coalesced loads
+//    through a ring of 4 tiles per warp (with 16 warps that is every tile of
+//    a CTA at the ffn_gate shape): the first 4 tiles are requested before the
+//    wait for the previous kernel, so their latency overlaps that wait, the
+//    transform and the table build; each consumed tile is replaced by the
+//    warp's next one.
+//  * Programmatic dependent launch: the kernel lets its successor launch after
+//    its table build and itself waits (griddepcontrol.wait) only before it
+//    reads x or writes any output.  Before the wait it issues what does not
+//    depend on the previous kernel: an L2 prefetch of its whole weight share,
+//    the first ring of tiles, the signs, and an L2 hint for the lines of x.
 #include <cuda_fp16.h>
 
 #include "bitlin_internal.cuh"
@@ -56,6 +57,9 @@ constexpr int kSmemTranspose = 16 * kPad * 4;           // 2112 B
 constexpr int kSmemSlice = (kSlice + kSlice / 32) * 4;  // 528 floats
 constexpr int kMaxList = 1024;                          // finished-tile list (ints)
 constexpr int kDecodeSmem = kLutBytes + kSmemTranspose + kSmemSlice + (kMaxList + 1) * 4;
+// Cluster split-K: the CTA's partial sums [M][tiles][32] follow, 16-byte aligned.
+constexpr int kPbufOff = (kDecodeSmem + 15) & ~15;
+constexpr int kMaxClusterSlices = 16;
 constexpr int kRowsPerWarp = 16 / kDecodeWarps;  // rows of the [16][32] transform view per warp
 static_assert(kDecodeWarps == 8 || kDecodeWarps == 16, "prologue mapping assumes 8 or 16 warps");
 
@@ -95,23 +99,51 @@ __device__ __forceinline__ int perm_source(int k)
 // Rotated activations of token m for slice s, in two parts so that the
 // caller can issue other loads between them.  Thread (warp w, lane q) covers
 // rows p = w and p = w + 8 of the [16][32] view of the half block.
-// slice_load: the raw x and sign values (gather through the ssm_out
+// The raw x and sign values of this thread (gather through the ssm_out
 // permutation when requested); no arithmetic, so nothing waits on them yet.
-__device__ __forceinline__ void slice_load(const DecodeParams& p, int m, int s, int warp, int lane,
-                                           float (&v)[4 * kRowsPerWarp])
+// The signs belong to the handle and may be read before the wait for the
+// previous kernel; x may not.
+__device__ __forceinline__ void slice_load_signs(const DecodeParams& p, int s, int warp, int lane,
+                                                 float (&v)[4 * kRowsPerWarp])
 {
     const int b = s >> 1;
-    const float* xm = p.x + (size_t)m * p.K;
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
-        const int i = 32 * (warp + kDecodeWarps * r) + lane;  // 0..511
-        const int k0 = b * 1024 + i, k1 = k0 + 512;
-        const int src0 = p.perm ? perm_source(k0) : k0;
-        const int src1 = p.perm ? perm_source(k1) : k1;
-        v[4 * r + 0] = __ldg(xm + src0);
+        const int k0 = b * 1024 + 32 * (warp + kDecodeWarps * r) + lane;  // i = 0..511
         v[4 * r + 1] = __ldg(p.signs + k0);
-        v[4 * r + 2] = __ldg(xm + src1);
-        v[4 * r + 3] = __ldg(p.signs + k1);
+        v[4 * r + 3] = __ldg(p.signs + k0 + 512);
+    }
+}
+
+__device__ __forceinline__ const float* x_source(const DecodeParams& p, int m, int k)
+{
+    return p.x + (size_t)m * p.K + (p.perm ? perm_source(k) : k);
+}
+
+__device__ __forceinline__ void slice_load_x(const DecodeParams& p, int m, int s, int warp, int lane,
+                                             float (&v)[4 * kRowsPerWarp])
+{
+    const int b = s >> 1;
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        const int k0 = b * 1024 + 32 * (warp + kDecodeWarps * r) + lane;
+        v[4 * r + 0] = __ldg(x_source(p, m, k0));
+        v[4 * r + 2] = __ldg(x_source(p, m, k0 + 512));
+    }
+}
+
+// A hint only: ask L2 for the lines of x this thread will read.  Issued
+// before the wait it has no effect on what is read after it.
+__device__ __forceinline__ void slice_prefetch_x(const DecodeParams& p, int m, int s, int warp, int lane)
+{
+    const int b = s >> 1;
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        const int k0 = b * 1024 + 32 * (warp + kDecodeWarps * r) + lane;
+        if (p.perm || lane == 0) {
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(x_source(p, m, k0)));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(x_source(p, m, k0 + 512)));
+        }
     }
 }
 
@@ -332,6 +364,57 @@ __device__ __forceinline__ void splitk_finish(const DecodeParams& p, int ta, int
     }
 }
 
+// ---- thread-block cluster (distributed shared memory) helpers --------------
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, int rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_cluster(uint32_t caddr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
+    return v;
+}
+
+// Split-K across a cluster: CTA rank s of the cluster holds slice s's partial
+// sums of the cluster's tiles [ta, tb) in its own shared memory (pbuf,
+// [M][tb - ta][32]).  After a cluster barrier each CTA sums an equal share of
+// the rows over all S CTAs, in slice order s = 0..S-1 (the same order and
+// arithmetic as the global-scratch path), and writes y.  A second barrier
+// keeps every CTA's shared memory alive until the others have read it.
+__device__ __forceinline__ void cluster_finish(const DecodeParams& p, int ta, int tb, int rank, const float* pbuf)
+{
+    cluster_sync();
+    const int ntile = tb - ta;
+    const int rows = p.M * ntile * kTileRows;
+    const int lo = (int)((long long)rows * rank / p.S), hi = (int)((long long)rows * (rank + 1) / p.S);
+    const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(pbuf));
+    for (int i = lo + (int)threadIdx.x; i < hi; i += kDecodeThreads) {
+        const uint32_t a = base + 4u * (uint32_t)i;
+        float v[kMaxClusterSlices];
+#pragma unroll
+        for (int j = 0; j < kMaxClusterSlices; ++j)
+            if (j < p.S) v[j] = ld_cluster(cluster_map(a, j));
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxClusterSlices; ++j)
+            if (j < p.S) sum += v[j];
+        const int m = i / (ntile * kTileRows), r = i - m * ntile * kTileRows;
+        const int n = ta * kTileRows + r;
+        if (n < p.N) p.y[(size_t)m * p.N + n] = sum;
+    }
+    cluster_sync();
+}
+
 __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -340,13 +423,21 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
     float* xs = tbuf + 16 * kPad;
     int* done_list = reinterpret_cast<int*>(xs + kSlice + kSlice / 32);  // [kMaxList]
     int* done_count = done_list + kMaxList;
+    float* pbuf = reinterpret_cast<float*>(smem + kPbufOff);  // cluster split-K only
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Units owned by this CTA, [u0, u1) in slice-major order.  With
     // ctas_per_slice > 0 every CTA stays inside one slice (one table build);
     // otherwise (more slices than CTAs) the units are split evenly.
     int u0, u1;
-    if (p.ctas_per_slice > 0) {
+    int rank = 0;  // cluster mode: this CTA's slice = its rank in the cluster
+    if (p.cluster) {
+        // Cluster c (consecutive blocks) covers tiles [T*c/ncl, T*(c+1)/ncl) of every slice.
+        const int ncl = gridDim.x / p.S, c = blockIdx.x / p.S;
+        rank = blockIdx.x - c * p.S;
+        u0 = rank * p.T + (int)((long long)p.T * c / ncl);
+        u1 = rank * p.T + (int)((long long)p.T * (c + 1) / ncl);
+    } else if (p.ctas_per_slice > 0) {
         const int s = blockIdx.x / p.ctas_per_slice, c = blockIdx.x - s * p.ctas_per_slice;
         u0 = s * p.T + (int)((long long)p.T * c / p.ctas_per_slice);
         u1 = s * p.T + (int)((long long)p.T * (c + 1) / p.ctas_per_slice);
@@ -367,8 +458,27 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
     prefetch_l2(p.bits + (size_t)u0 * 128, (size_t)(u1 - u0) * 2048, threadIdx.x);
     prefetch_l2(p.scales + (size_t)u0 * 32, (size_t)(u1 - u0) * 256, (threadIdx.x + 128) % kDecodeThreads);
 #endif
+    // Before the wait: this warp's first tiles (ta + warp + warps * j, j < kRing) and
+    // the signs of the first segment, whose latency then overlaps the wait, and
+    // the L2 hint for x.
+    uint4 rb[kRing][4];
+    uint2 rs[kRing];
+    float xv[4 * kRowsPerWarp];
+    {
+        const int s = u0 / p.T, ta = u0 - s * p.T, tb = min(p.T, ta + (u1 - u0));
+#pragma unroll
+        for (int d = 0; d < kRing; ++d) {
+            const int t = ta + warp + kDecodeWarps * d;
+            if (u0 < u1 && t < tb) load_tile(p, s, t, lane, rb[d], rs[d]);
+        }
+        if (u0 < u1) {
+            slice_load_signs(p, s, warp, lane, xv);
+            slice_prefetch_x(p, 0, s, warp, lane);
+        }
+    }
     pdl_wait();
     bool triggered = false;
+    bool preloaded = true;  // the ring and the signs hold the first (segment, token)
 
     for (int u = u0; u < u1;) {
         const int s = u / p.T;
@@ -378,19 +488,17 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
 
         for (int m = 0; m < p.M; ++m) {
             __syncthreads();  // the previous table is no longer read
-            // x first, alone, so that its loads are not queued behind the tile
-            // loads; then this warp's first tiles ta + warp + 8j, j < kRing,
-            // whose latency overlaps the transform and the table build.
-            float xv[4 * kRowsPerWarp];
-            slice_load(p, m, s, warp, lane, xv);
-            slice_transform_rows(s, xv, tbuf, warp, lane);
-            uint4 rb[kRing][4];
-            uint2 rs[kRing];
+            if (!preloaded) {
+                slice_load_signs(p, s, warp, lane, xv);
 #pragma unroll
-            for (int d = 0; d < kRing; ++d) {
-                const int t = ta + warp + kDecodeWarps * d;
-                if (t < tb) load_tile(p, s, t, lane, rb[d], rs[d]);
+                for (int d = 0; d < kRing; ++d) {
+                    const int t = ta + warp + kDecodeWarps * d;
+                    if (t < tb) load_tile(p, s, t, lane, rb[d], rs[d]);
+                }
             }
+            preloaded = false;
+            slice_load_x(p, m, s, warp, lane, xv);
+            slice_transform_rows(s, xv, tbuf, warp, lane);
             __syncthreads();
             slice_transform_cols(tbuf, xs, warp, lane);
             __syncthreads();
@@ -402,7 +510,10 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
                 pdl_launch_dependents();
                 triggered = true;
             }
-            float* part = p.partials + ((size_t)s * p.M + m) * npad;
+            // Partial sums: tile t, lane -> part[(t - tbase) * 32 + lane].
+            float* part = p.cluster ? pbuf + (size_t)m * (tb - ta) * kTileRows
+                                    : p.partials + ((size_t)s * p.M + m) * npad;
+            const int tbase = p.cluster ? ta : 0;
             for (int j0 = 0;; j0 += kRing) {
                 bool more = true;
 #pragma unroll
@@ -418,15 +529,50 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
                     const int tn0 = t0 + kDecodeWarps * kRing, tn1 = t1 + kDecodeWarps * kRing;
                     if (tn0 < tb) load_tile(p, s, tn0, lane, rb[d], rs[d]);
                     if (tn1 < tb) load_tile(p, s, tn1, lane, rb[d + 1], rs[d + 1]);
-                    part[(size_t)t0 * kTileRows + lane] = v0;
-                    if (t1 < tb) part[(size_t)t1 * kTileRows + lane] = v1;
+                    part[(size_t)(t0 - tbase) * kTileRows + lane] = v0;
+                    if (t1 < tb) part[(size_t)(t1 - tbase) * kTileRows + lane] = v1;
                 }
                 if (!more) break;
             }
         }
-        splitk_finish(p, ta, tb, npad, done_list, done_count, reinterpret_cast<float*>(lut));
+        if (p.cluster)
+            cluster_finish(p, ta, tb, rank, pbuf);
+        else
+            splitk_finish(p, ta, tb, npad, done_list, done_count, reinterpret_cast<float*>(lut));
     }
     if (!triggered) pdl_launch_dependents();
+}
+
+}  // namespace
+
+namespace {
+
+// Clusters of S CTAs (one CTA per SM) that can be resident at once, by S;
+// 0 = not queried yet, -1 = none.
+int g_max_clusters[kMaxClusterSlices + 1];
+int g_max_smem = 0;  // opt-in shared memory per block of the device
+
+int max_clusters(int S, int num_sms)
+{
+    if (g_max_clusters[S] != 0) return g_max_clusters[S];
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S * (num_sms / S));
+    cfg.blockDim = dim3(kDecodeThreads);
+    cfg.dynamicSmemBytes = g_max_smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, bitlin_decode_gemv, &cfg) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        n = -1;
+    }
+    g_max_clusters[S] = n;
+    return n;
 }
 
 }  // namespace
@@ -435,32 +581,61 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
 {
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(bitlin_decode_gemv, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kDecodeSmem);
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess && g_max_smem < kDecodeSmem) e = cudaErrorInvalidConfiguration;
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(bitlin_decode_gemv, cudaFuncAttributeMaxDynamicSharedMemorySize, g_max_smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(bitlin_decode_gemv, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     DecodeParams q = p;
-    int grid;
-    if (p.S <= num_sms) {
-        q.ctas_per_slice = num_sms / p.S < p.T ? num_sms / p.S : p.T;
-        grid = p.S * q.ctas_per_slice;
-    } else {
-        const long long U = (long long)p.S * p.T;
-        q.ctas_per_slice = 0;
-        grid = (int)(U < num_sms ? U : num_sms);
+    int grid, smem = kDecodeSmem, cluster = 0;
+    q.cluster = 0;
+    // Split-K across a cluster when the slices fit one (S <= 16) and the
+    // partial sums fit shared memory; else through the global scratch.
+    if (p.allow_cluster && p.S <= kMaxClusterSlices) {
+        const int maxc = max_clusters(p.S, num_sms);
+        if (maxc > 0) {
+            const int ncl = maxc < p.T ? maxc : p.T;
+            const long long pb = (long long)p.M * ((p.T + ncl - 1) / ncl) * kTileRows * 4;
+            if (kPbufOff + pb <= g_max_smem) {
+                q.cluster = 1;
+                q.ctas_per_slice = ncl;
+                grid = p.S * ncl;
+                smem = kPbufOff + (int)pb;
+                cluster = p.S;
+            }
+        }
+    }
+    if (!q.cluster) {
+        if (p.S <= num_sms) {
+            q.ctas_per_slice = num_sms / p.S < p.T ? num_sms / p.S : p.T;
+            grid = p.S * q.ctas_per_slice;
+        } else {
+            const long long U = (long long)p.S * p.T;
+            q.ctas_per_slice = 0;
+            grid = (int)(U < num_sms ? U : num_sms);
+        }
     }
 
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kDecodeThreads);
-    cfg.dynamicSmemBytes = kDecodeSmem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = cluster ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, bitlin_decode_gemv, q);
 }
