@@ -42,6 +42,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ffn_gate")
+    ap.add_argument("--op", choices=["gemv", "mlp", "embed"], default="gemv",
+                    help="gemv: one folded product per step (the headline); mlp: the MLP block "
+                         "(gate+up 5120x34816, SiLU, down 17408x5120) per step; embed: M embedding "
+                         "lookups with the inverse rotation in a 248,320 x 5120 table per step")
     ap.add_argument("--M", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
@@ -255,6 +259,197 @@ def run_reference(args, w: synth.Workload):
     print(json.dumps(line), flush=True)
 
 
+MLP_METRIC = "MLP block tokens/s and weight GB/s (1-bit WHT-folded gate+up 5120x34816, SiLU, down 17408x5120)"
+EMBED_METRIC = "embedding lookups/s with the inverse rotation (1-bit WHT-folded table 248320x5120)"
+
+
+def timed_graph(step, stream, steps: int, warmup: int, pg, dev):
+    """Warm up, capture `step` calls in CUDA graphs, replay exactly `steps` calls between a
+    barrier and device synchronizes; CUDA events on `stream`.  Returns (ms, clocks)."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+    stream.synchronize()
+    chunk = min(256, max(1, steps))
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    step(i)
+        return g
+
+    full, rem = divmod(steps, chunk)
+    g_chunk = capture(chunk) if full else None
+    g_rem = capture(rem) if rem else None
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(full):
+            g_chunk.replay()
+        if g_rem:
+            g_rem.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    return max_over_ranks(ev0.elapsed_time(ev1), pg, dev), clocks
+
+
+def run_op(args, ws, rank, local, pg):
+    """--op mlp / --op embed: the NEXT operations on the same kernels, one JSON line."""
+    import torch
+
+    import hadamard_rotated_binary_gb300 as hrb
+    from hadamard_rotated_binary_gb300 import build as hbuild
+
+    hbuild.build()
+    dev = torch.device("cuda", local)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    M = args.M or 1
+    stream = torch.cuda.Stream(device=dev)
+    peaks, peak_kind = measured_peaks()
+    if args.op == "mlp":
+        wgu, wdn = synth.workload("gate_up", M), synth.workload("ffn_down", M)
+        gu_in, dn_in = synth.make_inputs(wgu), synth.make_inputs(wdn)
+        wbytes = wgu.weight_bytes() + wdn.weight_bytes()
+        R = args.copies if args.copies else max(2, -(-4 * l2 // wbytes))
+
+        def dev_layer(inp):
+            b, sc, sg, _ = inp
+            return hrb.BitLinear(torch.from_numpy(b.view(np.int32)).to(dev),
+                                 torch.from_numpy(sc.view(np.int16)).to(dev), torch.from_numpy(sg).to(dev), 0)
+
+        pairs = [(dev_layer(gu_in), dev_layer(dn_in)) for _ in range(R)]
+        x = gu_in[3]
+        xd = torch.from_numpy(x).to(dev)
+        yd = torch.empty((M, wdn.N), dtype=torch.float32, device=dev)
+
+        def step(i):
+            hrb.mlp_forward(pairs[i % R][0], pairs[i % R][1], xd, out=yd, stream=stream)
+
+        ms, clocks = timed_graph(step, stream, args.steps, max(args.warmup, R), pg, dev)
+        s_step = ms / 1e3 / args.steps
+        algo = wbytes + 4 * M * wgu.K + 4 * M * wdn.N + 4 * (wgu.K + wdn.K)
+        flops = 2.0 * M * (wgu.N * wgu.K + wdn.N * wdn.K)
+        if M == 1:
+            roof = {"bound": "hbm", "achieved": algo / s_step / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "kernel": "bitlin_decode_gemv (x2)", "bytes_per_launch": algo}
+        else:
+            digits = 3 if M < 64 else 1
+            roof = {"bound": "tensor", "achieved": digits * flops / s_step / 1e12, "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "kernel": "bitlin_tc_gemm (x2)", "flops_per_launch": digits * flops}
+        roof.update({"frac": roof["achieved"] / roof["peak"], "peak_kind": peak_kind, "traffic": None})
+        metric, config = MLP_METRIC, {"workload": "mlp_block", "M": M, "hidden": wgu.K, "ffn": wdn.K,
+                                      "weight_copies": R, "weight_set_bytes": R * wbytes,
+                                      "l2": f"inputs larger than L2: {R} distinct weight pairs cycled"}
+        launches = 2 if M == 1 else 4
+        wgb = wbytes / s_step / 1e9
+
+        def e2e_call(xh, yh):
+            xd.copy_(xh, non_blocking=True)
+            hrb.mlp_forward(pairs[0][0], pairs[0][1], xd, out=yd)
+            yh.copy_(yd, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        h2d, d2h, out_shape = 4 * M * wgu.K, 4 * M * wdn.N, (M, wdn.N)
+
+        def cpu_call():
+            import oracle
+
+            oracle.build()
+            return lambda: oracle.mlp(gu_in[:3] + (0,), dn_in[:3] + (0,), x)
+    else:
+        N, K = 248320, 5120
+        seed = 0xB1711A00 + 12
+        bits = synth.random_bits(seed, N, K)
+        scales = synth.random_scales(seed, N, K, 0.005, 0.03)
+        signs = synth.random_signs(seed, K)
+        layer = hrb.BitLinear(torch.from_numpy(bits.view(np.int32)).to(dev),
+                              torch.from_numpy(scales.view(np.int16)).to(dev), torch.from_numpy(signs).to(dev), 0)
+        nsets = 64
+        ids = (synth.stream(seed, 5, nsets * M) % np.uint64(N)).astype(np.int32).reshape(nsets, M)
+        idd = torch.from_numpy(ids).to(dev)
+        yd = torch.empty((M, K), dtype=torch.float32, device=dev)
+
+        def step(i):
+            layer.embed(idd[i % nsets], out=yd, stream=stream)
+
+        ms, clocks = timed_graph(step, stream, args.steps, max(args.warmup, 3), pg, dev)
+        s_step = ms / 1e3 / args.steps
+        row = K // 8 + 2 * (K // 128)
+        algo = M * (row + 4 + 4 * K) + 4 * K
+        roof = {"bound": "hbm", "achieved": algo / s_step / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "kernel": "bitlin_embed_rows", "bytes_per_launch": algo}
+        roof.update({"frac": roof["achieved"] / roof["peak"], "peak_kind": peak_kind, "traffic": None})
+        metric, config = EMBED_METRIC, {"workload": "embed", "M": M, "N": N, "K": K,
+                                        "l2": f"table of {N * row / 1e6:.0f} MB > L2; {nsets} id sets of random rows"}
+        launches, wgb = 1, M * row / s_step / 1e9
+        x = ids[0]
+
+        def e2e_call(xh, yh):
+            idd[0].copy_(xh, non_blocking=True)
+            layer.embed(idd[0], out=yd)
+            yh.copy_(yd, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        h2d, d2h, out_shape = 4 * M, 4 * M * K, (M, K)
+
+        def cpu_call():
+            import oracle
+
+            oracle.build()
+            return lambda: oracle.embed(bits, scales, signs, ids[0])
+
+    # end to end through the Python API: pinned host input -> device, call, device -> pinned host
+    xh = torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    yh = torch.empty(out_shape, dtype=torch.float32).pin_memory()
+    e2e_steps = min(args.steps, args.e2e_steps)
+    for _ in range(3):
+        e2e_call(xh, yh)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_call(xh, yh)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, pg, dev)
+    if rank != 0:
+        return
+    line = {
+        "metric": metric, "value": ws * M / s_step, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64: Bernoulli(0.5) bits, U[0.005,0.03] fp16 scales, +-1 signs, N(0,1) x)",
+        "config": config, "weight_gbs": wgb, "roofline": roof, "gpu_launches": args.steps * launches,
+        "clocks": clocks,
+        "e2e": {"value": ws * M * e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "api": "python binding, pinned host buffers"},
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+
+        fn = cpu_call()
+        n, t0 = 0, time.perf_counter()
+        while True:
+            fn()
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= args.cpu_seconds:
+                break
+        line["cpu_baseline"] = {"value": n * M / el, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                                "sample": f"{n} whole oracle calls in {el:.1f} s, f64"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     ws, rank, local = dist_env()
@@ -274,6 +469,11 @@ def main():
 
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
         pg = dist
+    if args.op != "gemv":
+        run_op(args, ws, rank, local, pg)
+        if pg:
+            pg.destroy_process_group()
+        return
 
     import hadamard_rotated_binary_gb300 as hrb
     from hadamard_rotated_binary_gb300 import build as hbuild

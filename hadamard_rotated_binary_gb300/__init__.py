@@ -15,6 +15,7 @@ from __future__ import annotations
 
 from ._binding import (  # noqa: F401
     BITLIN_EDEVICE,
+    BITLIN_EINDEX,
     BITLIN_ESCRATCH,
     BITLIN_EINVAL,
     BITLIN_ENOMEM,
@@ -32,11 +33,13 @@ from ._binding import (  # noqa: F401
     header_functions,
     lib,
     library_path,
+    mlp_forward,
 )
 
 __all__ = [
     "BitLinear",
     "BitlinError",
+    "mlp_forward",
     "lib",
     "library_path",
     "header_functions",

@@ -16,6 +16,7 @@ BITLIN_ECUDA = 3
 BITLIN_ETIMEOUT = 4
 BITLIN_EDEVICE = 5
 BITLIN_ESCRATCH = 6
+BITLIN_EINDEX = 7
 
 PERM_NONE = 0
 PERM_SSM_TILED_TO_GROUPED = 1
@@ -64,6 +65,8 @@ def lib() -> ctypes.CDLL:
     L.bitlin_forward_noalloc.argtypes = [P, P, i32, P, P]
     L.bitlin_forward_noalloc.restype = i32
     L.bitlin_noalloc_scratch_bytes.restype = ctypes.c_size_t
+    L.bitlin_embed.argtypes = [P, P, i32, P, P]
+    L.bitlin_mlp_forward.argtypes = [P, P, P, i32, P, P]
     L.bitlin_set_path.argtypes = [P, i32]
     L.bitlin_set_wait_budget.argtypes = [P, i64]
     L.bitlin_test_stall.argtypes = [P, i32]
@@ -72,7 +75,7 @@ def lib() -> ctypes.CDLL:
     L.bitlin_cuda_error.argtypes = [P]
     L.bitlin_status_string.argtypes = [i32]
     L.bitlin_status_string.restype = ctypes.c_char_p
-    for name in ("bitlin_create", "bitlin_forward", "bitlin_forward_host", "bitlin_set_path",
+    for name in ("bitlin_create", "bitlin_forward", "bitlin_forward_host", "bitlin_embed", "bitlin_mlp_forward", "bitlin_set_path",
                  "bitlin_set_wait_budget", "bitlin_test_stall", "bitlin_destroy", "bitlin_get_error",
                  "bitlin_cuda_error", "bitlin_version"):
         getattr(L, name).restype = i32
@@ -86,6 +89,22 @@ def _stream_handle(stream) -> int:
     if stream is None:
         stream = torch.cuda.current_stream()
     return int(stream.cuda_stream)
+
+
+def mlp_forward(gate_up: "BitLinear", down: "BitLinear", x, out=None, stream=None):
+    """bitlin_mlp_forward: down(silu(gate) * up) with [gate | up] = gate_up(x)."""
+    import torch
+
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous() or x.dim() != 2:
+        raise ValueError("x must be a contiguous float32 CUDA tensor [M][K]")
+    M = int(x.shape[0])
+    if out is None:
+        out = torch.empty((M, down.N), dtype=torch.float32, device=x.device)
+    st = lib().bitlin_mlp_forward(gate_up.handle, down.handle, x.data_ptr(), M, out.data_ptr(),
+                                  _stream_handle(stream))
+    if st != BITLIN_OK:
+        raise BitlinError(st, "bitlin_mlp_forward", lib().bitlin_cuda_error(down.handle))
+    return out
 
 
 class BitLinear:
@@ -157,6 +176,20 @@ class BitLinear:
         M = int(x.shape[0])
         self._check(lib().bitlin_forward_noalloc(self._h, x.data_ptr(), M, out.data_ptr(),
                                                  _stream_handle(stream)), "bitlin_forward_noalloc")
+        return out
+
+    def embed(self, ids, out=None, stream=None):
+        """bitlin_embed: rows ids (int32 CUDA tensor [M]) of the matrix, dequantized and
+        inverse-rotated, as float32 [M][K]."""
+        import torch
+
+        if ids.dtype != torch.int32 or not ids.is_cuda or not ids.is_contiguous() or ids.dim() != 1:
+            raise ValueError("ids must be a contiguous int32 CUDA tensor [M]")
+        M = int(ids.shape[0])
+        if out is None:
+            out = torch.empty((M, self.K), dtype=torch.float32, device=ids.device)
+        self._check(lib().bitlin_embed(self._h, ids.data_ptr(), M, out.data_ptr(), _stream_handle(stream)),
+                    "bitlin_embed")
         return out
 
     def set_path(self, path: int):

@@ -46,6 +46,7 @@ void release(bitlin_t h)
     free_dev(h->dev_error);
     free_dev(h->hx);
     free_dev(h->hy);
+    free_dev(h->mlp_in);
     if (h->h_err) cudaFreeHost(h->h_err);
     h->h_err = nullptr;
 }
@@ -108,7 +109,7 @@ bitlin_status ensure_xt(bitlin_t h, int M, int exact)
     return BITLIN_OK;
 }
 
-bitlin_status run_decode(bitlin_t h, const float* x, int M, float* y, cudaStream_t s)
+bitlin_status run_decode(bitlin_t h, const float* x, int M, float* y, cudaStream_t s, int swiglu = 0)
 {
     cudaError_t e = ensure_partials(h, M);
     if (e != cudaSuccess) return from_cuda(h, e);
@@ -129,14 +130,15 @@ bitlin_status run_decode(bitlin_t h, const float* x, int M, float* y, cudaStream
     p.ctas_per_slice = 0;
     p.cluster = 0;
     p.allow_cluster = 1;
+    p.swiglu = swiglu;
     return from_cuda(h, bitlin_launch_decode(p, h->num_sms, s));
 }
 
-bitlin_status run_tc(bitlin_t h, const float* x, int M, float* y, cudaStream_t s, int exact)
+bitlin_status run_tc(bitlin_t h, const float* x, int M, float* y, cudaStream_t s, int exact, int swiglu = 0)
 {
     bitlin_status st = ensure_xt(h, M, exact);
     if (st != BITLIN_OK) return st;
-    cudaError_t e = bitlin_launch_rotate_bf16(x, h->signs, M, h->K, h->perm, exact, h->xt, s);
+    cudaError_t e = bitlin_launch_rotate_bf16(x, h->signs, M, h->K, h->perm, exact, swiglu, h->xt, s);
     if (e != cudaSuccess) return from_cuda(h, e);
     PrefillParams p;
     p.bits = h->pbits;
@@ -168,6 +170,7 @@ const char* bitlin_status_string(bitlin_status s)
     case BITLIN_ETIMEOUT: return "a bounded device wait timed out";
     case BITLIN_EDEVICE: return "the current device is not an sm_103 GPU";
     case BITLIN_ESCRATCH: return "the call needs more scratch than the fixed no-alloc array holds";
+    case BITLIN_EINDEX: return "a token id is outside [0, N)";
     }
     return "unknown status";
 }
@@ -299,19 +302,51 @@ bitlin_status bitlin_test_stall(bitlin_t h, int on)
     return BITLIN_OK;
 }
 
+namespace {
+
+// The handle's path for M tokens (BITLIN_PATH_AUTO resolved).
+int choose_path(bitlin_t h, int M)
+{
+    if (h->path != BITLIN_PATH_AUTO) return h->path;
+    return M >= kPrefillMinM ? BITLIN_PATH_PREFILL : M >= 2 ? BITLIN_PATH_TC_EXACT : BITLIN_PATH_DECODE;
+}
+
+bitlin_status run_path(bitlin_t h, const float* x, int M, float* y, cudaStream_t s, int swiglu)
+{
+    switch (choose_path(h, M)) {
+    case BITLIN_PATH_PREFILL: return run_tc(h, x, M, y, s, 0, swiglu);
+    case BITLIN_PATH_TC_EXACT: return run_tc(h, x, M, y, s, 1, swiglu);
+    default: return run_decode(h, x, M, y, s, swiglu);
+    }
+}
+
+}  // namespace
+
 bitlin_status bitlin_forward(bitlin_t h, const float* x, int M, float* y, bitlin_stream_t stream)
 {
     if (!h || !x || !y || M < 1) return BITLIN_EINVAL;
     if (h->sticky != BITLIN_OK) return h->sticky;
+    return run_path(h, x, M, y, reinterpret_cast<cudaStream_t>(stream), 0);
+}
+
+bitlin_status bitlin_mlp_forward(bitlin_t gate_up, bitlin_t down, const float* x, int M, float* y,
+                                 bitlin_stream_t stream)
+{
+    if (!gate_up || !down || !x || !y || M < 1) return BITLIN_EINVAL;
+    if (gate_up->N != 2 * down->K || gate_up->device != down->device) return BITLIN_EINVAL;
+    if (gate_up->sticky != BITLIN_OK) return gate_up->sticky;
+    if (down->sticky != BITLIN_OK) return down->sticky;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int path = h->path;
-    if (path == BITLIN_PATH_AUTO)
-        path = M >= kPrefillMinM ? BITLIN_PATH_PREFILL : M >= 2 ? BITLIN_PATH_TC_EXACT : BITLIN_PATH_DECODE;
-    switch (path) {
-    case BITLIN_PATH_PREFILL: return run_tc(h, x, M, y, s, 0);
-    case BITLIN_PATH_TC_EXACT: return run_tc(h, x, M, y, s, 1);
-    default: return run_decode(h, x, M, y, s);
+    if (!down->mlp_in || down->mlp_M < M) {
+        free_dev(down->mlp_in);
+        down->mlp_M = 0;
+        cudaError_t e = cudaMalloc(&down->mlp_in, (size_t)M * gate_up->N * sizeof(float));
+        if (e != cudaSuccess) return from_cuda(down, e);
+        down->mlp_M = M;
     }
+    bitlin_status st = run_path(gate_up, x, M, down->mlp_in, s, 0);
+    if (st != BITLIN_OK) return st;
+    return run_path(down, down->mlp_in, M, y, s, 1);
 }
 
 bitlin_status bitlin_forward_host(bitlin_t h, const float* x_host, int M, float* y_host,
@@ -351,7 +386,20 @@ bitlin_status bitlin_get_error(bitlin_t h)
     e = cudaMemcpy(&v, h->dev_error, sizeof(int), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return from_cuda(h, e);
     if (v == kDevErrTimeout) h->sticky = BITLIN_ETIMEOUT;
+    if (v == kDevErrIndex && h->sticky == BITLIN_OK) {
+        e = cudaMemset(h->dev_error, 0, sizeof(int));
+        if (e != cudaSuccess) return from_cuda(h, e);
+        return BITLIN_EINDEX;
+    }
     return h->sticky;
+}
+
+bitlin_status bitlin_embed(bitlin_t h, const int32_t* ids, int M, float* out, bitlin_stream_t stream)
+{
+    if (!h || !ids || !out || M < 1) return BITLIN_EINVAL;
+    if (h->sticky != BITLIN_OK) return h->sticky;
+    return from_cuda(h, bitlin_launch_embed(h->pbits, h->pscales, h->signs, ids, M, h->N, h->K, out,
+                                            h->dev_error, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int bitlin_cuda_error(bitlin_t h) { return h ? h->last_cuda_error : 0; }

@@ -30,6 +30,7 @@ constexpr int kPrefillMinM = 64;      // auto path switch
 
 // Device-side error word values (bitlin_t::dev_error).
 constexpr int kDevErrTimeout = 1;
+constexpr int kDevErrIndex = 2;      // a token id outside [0, N) (embedding lookup)
 
 struct DecodeParams {
     const uint4* bits;      // [S][T][4][32] uint4 (repacked, see repack.cu)
@@ -43,6 +44,7 @@ struct DecodeParams {
     int ctas_per_slice;     // set by the launcher
     int cluster;            // set by the launcher: 1 = split-K summed across a thread-block cluster
     int allow_cluster;      // set by the caller: 0 keeps the split-K in the global scratch
+    int swiglu;             // 1: x is [M][2K] (gate | up); the GEMV's input is silu(gate) * up
 };
 
 struct PrefillParams {
@@ -88,6 +90,11 @@ struct bitlin {
     long long wait_budget_ns = 0;
     int stall_test = 0;
 
+    // MLP block (bitlin_mlp_forward on the down-projection handle): the gate and
+    // up outputs [M][2K] that the down projection reads through SiLU
+    float* mlp_in = nullptr;
+    int mlp_M = 0;
+
     // host-buffer entry point staging
     float* hx = nullptr;
     float* hy = nullptr;
@@ -101,8 +108,11 @@ cudaError_t bitlin_launch_repack_prefill(const uint32_t* bits, int N, int K, uin
                                          cudaStream_t s);
 cudaError_t bitlin_launch_check_signs(const float* signs, int K, int* bad, cudaStream_t s);
 cudaError_t bitlin_launch_decode(const bitlin_impl::DecodeParams& p, int num_sms, cudaStream_t s);
+cudaError_t bitlin_launch_embed(const uint32_t* bits, const uint16_t* scales, const float* signs,
+                                const int32_t* ids, int M, int N, int K, float* out, int* dev_error,
+                                cudaStream_t s);
 cudaError_t bitlin_launch_rotate_bf16(const float* x, const float* signs, int M, int K, int perm,
-                                      int digits, void* xt, cudaStream_t s);
+                                      int digits, int swiglu, void* xt, cudaStream_t s);
 cudaError_t bitlin_launch_prefill(const bitlin_impl::PrefillParams& p, const void* tmap,
                                   const void* tmap_bits, int stall_test, cudaStream_t s);
 cudaError_t bitlin_launch_tc_exact(const bitlin_impl::PrefillParams& p, const void* tmap,

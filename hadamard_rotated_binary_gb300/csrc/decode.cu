@@ -115,10 +115,15 @@ __device__ __forceinline__ void slice_load_signs(const DecodeParams& p, int s, i
     }
 }
 
+// Input element k of token m (after the permutation).  With swiglu set, x
+// holds [M][2K] gate and up values and the input is silu(gate) * up, SiLU(g)
+// = g / (1 + e^-g) in f32 ("Inside the One-Bit Engine", MLP station).
 __device__ __forceinline__ const float* x_source(const DecodeParams& p, int m, int k)
 {
-    return p.x + (size_t)m * p.K + (p.perm ? perm_source(k) : k);
+    return p.x + (size_t)m * (p.swiglu ? 2 * p.K : p.K) + (p.perm ? perm_source(k) : k);
 }
+
+__device__ __forceinline__ float swiglu(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
 __device__ __forceinline__ void slice_load_x(const DecodeParams& p, int m, int s, int warp, int lane,
                                              float (&v)[4 * kRowsPerWarp])
@@ -127,8 +132,15 @@ __device__ __forceinline__ void slice_load_x(const DecodeParams& p, int m, int s
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
         const int k0 = b * 1024 + 32 * (warp + kDecodeWarps * r) + lane;
-        v[4 * r + 0] = __ldg(x_source(p, m, k0));
-        v[4 * r + 2] = __ldg(x_source(p, m, k0 + 512));
+        const float* a0 = x_source(p, m, k0);
+        const float* a1 = x_source(p, m, k0 + 512);
+        if (p.swiglu) {
+            v[4 * r + 0] = swiglu(__ldg(a0), __ldg(a0 + p.K));
+            v[4 * r + 2] = swiglu(__ldg(a1), __ldg(a1 + p.K));
+        } else {
+            v[4 * r + 0] = __ldg(a0);
+            v[4 * r + 2] = __ldg(a1);
+        }
     }
 }
 
@@ -143,6 +155,10 @@ __device__ __forceinline__ void slice_prefetch_x(const DecodeParams& p, int m, i
         if (p.perm || lane == 0) {
             asm volatile("prefetch.global.L2 [%0];" ::"l"(x_source(p, m, k0)));
             asm volatile("prefetch.global.L2 [%0];" ::"l"(x_source(p, m, k0 + 512)));
+            if (p.swiglu) {
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(x_source(p, m, k0) + p.K));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(x_source(p, m, k0 + 512) + p.K));
+            }
         }
     }
 }
@@ -273,11 +289,17 @@ __device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes, int tid
 }
 
 // Tiles in flight per warp: the register ring of prefetched tiles (even).
-constexpr int kRing = 4;
+#ifndef BITLIN_DECODE_RING
+#define BITLIN_DECODE_RING 4
+#endif
+constexpr int kRing = BITLIN_DECODE_RING;
 
 // Registers per thread: with 8 warps per CTA two CTAs (this call's and the
 // next call's) fit in an SM's 65,536 registers.
-constexpr int kDecodeRegs = 128;
+#ifndef BITLIN_DECODE_REGS
+#define BITLIN_DECODE_REGS 128
+#endif
+constexpr int kDecodeRegs = BITLIN_DECODE_REGS;
 
 // End of a segment [ta, tb) of one slice: publish the partial sums, take one
 // ticket per tile (in parallel, one thread each), and reduce the tiles whose
@@ -547,8 +569,13 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
 
 namespace {
 
-// Clusters of S CTAs (one CTA per SM) that can be resident at once, by S;
-// 0 = not queried yet, -1 = none.
+// Cluster launches reserve this much shared memory for the partial sums.
+constexpr int kPbufBytes = 16384;
+
+// Clusters of S CTAs that one call may use, by S: the clusters that can be
+// resident at once divided by the CTAs that fit on an SM, so that when two
+// fit, the next call's CTAs find room beside this call's and start their
+// weight prefetch early.  0 = not queried yet, -1 = none.
 int g_max_clusters[kMaxClusterSlices + 1];
 int g_max_smem = 0;  // opt-in shared memory per block of the device
 
@@ -563,14 +590,18 @@ int max_clusters(int S, int num_sms)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S * (num_sms / S));
     cfg.blockDim = dim3(kDecodeThreads);
-    cfg.dynamicSmemBytes = g_max_smem;
+    cfg.dynamicSmemBytes = kPbufOff + kPbufBytes;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, bitlin_decode_gemv, &cfg) != cudaSuccess || n < 1) {
+    int n = 0, per_sm = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, bitlin_decode_gemv, &cfg) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bitlin_decode_gemv, kDecodeThreads,
+                                                      kPbufOff + kPbufBytes) != cudaSuccess) {
         (void)cudaGetLastError();
-        n = -1;
+        n = 0;
     }
+    if (per_sm > 1) n /= per_sm;
+    if (n < 1) n = -1;
     g_max_clusters[S] = n;
     return n;
 }
@@ -602,11 +633,11 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
         if (maxc > 0) {
             const int ncl = maxc < p.T ? maxc : p.T;
             const long long pb = (long long)p.M * ((p.T + ncl - 1) / ncl) * kTileRows * 4;
-            if (kPbufOff + pb <= g_max_smem) {
+            if (pb <= kPbufBytes) {
                 q.cluster = 1;
                 q.ctas_per_slice = ncl;
                 grid = p.S * ncl;
-                smem = kPbufOff + (int)pb;
+                smem = kPbufOff + kPbufBytes;
                 cluster = p.S;
             }
         }

@@ -99,6 +99,7 @@ extern "C" bitlin_status bitlin_forward_noalloc(bitlin_t h, const float* x, int 
             p.ctas_per_slice = 0;
             p.cluster = 0;
             p.allow_cluster = 0;  // this entry point's split-K goes through the static scratch
+            p.swiglu = 0;
             e = bitlin_launch_decode(p, h->num_sms, s);
         }
     }

@@ -27,7 +27,7 @@ __device__ __forceinline__ int perm_source(int k)
 
 __global__ void __launch_bounds__(256) bitlin_rotate_bf16(const float* __restrict__ x,
                                                           const float* __restrict__ signs, int M,
-                                                          int K, int perm, int digits,
+                                                          int K, int perm, int digits, int swiglu,
                                                           __nv_bfloat16* __restrict__ xt)
 {
     const int lane = threadIdx.x & 31;
@@ -35,14 +35,21 @@ __global__ void __launch_bounds__(256) bitlin_rotate_bf16(const float* __restric
     const int B = K / 1024;
     if (gw >= (long long)M * B) return;
     const int m = (int)(gw / B), b = (int)(gw - (long long)m * B);
-    const float* xm = x + (size_t)m * K;
+    // With swiglu set, x is [M][2K] gate | up and the input is silu(gate) * up,
+    // SiLU(g) = g / (1 + e^-g) in f32 ("Inside the One-Bit Engine", MLP station).
+    const float* xm = x + (size_t)m * (swiglu ? 2 * K : K);
 
     float v[32];
 #pragma unroll
     for (int p = 0; p < 32; ++p) {
         const int k = b * 1024 + 32 * p + lane;
         const int src = perm ? perm_source(k) : k;
-        v[p] = __ldg(xm + src) * __ldg(signs + k);
+        float a = __ldg(xm + src);
+        if (swiglu) {
+            const float u = __ldg(xm + K + src);
+            a = a / (1.f + expf(-a)) * u;
+        }
+        v[p] = a * __ldg(signs + k);
     }
 #pragma unroll
     for (int st = 1; st < 32; st <<= 1) {
@@ -88,12 +95,12 @@ __global__ void __launch_bounds__(256) bitlin_rotate_bf16(const float* __restric
 }  // namespace
 
 cudaError_t bitlin_launch_rotate_bf16(const float* x, const float* signs, int M, int K, int perm,
-                                      int digits, void* xt, cudaStream_t s)
+                                      int digits, int swiglu, void* xt, cudaStream_t s)
 {
     const long long warps = (long long)M * (K / 1024);
     const int threads = 256;
     const long long blocks = (warps * 32 + threads - 1) / threads;
-    bitlin_rotate_bf16<<<(unsigned)blocks, threads, 0, s>>>(x, signs, M, K, perm, digits,
+    bitlin_rotate_bf16<<<(unsigned)blocks, threads, 0, s>>>(x, signs, M, K, perm, digits, swiglu,
                                                            static_cast<__nv_bfloat16*>(xt));
     return cudaGetLastError();
 }

@@ -60,7 +60,8 @@ typedef enum {
     BITLIN_ECUDA = 3,    /* a CUDA runtime call or kernel launch failed (see bitlin_cuda_error) */
     BITLIN_ETIMEOUT = 4, /* a bounded wait inside a kernel gave up; the output is not valid */
     BITLIN_EDEVICE = 5,  /* the current device is not an sm_103 GPU */
-    BITLIN_ESCRATCH = 6  /* bitlin_forward_noalloc: the call needs more than its fixed scratch */
+    BITLIN_ESCRATCH = 6, /* bitlin_forward_noalloc: the call needs more than its fixed scratch */
+    BITLIN_EINDEX = 7    /* bitlin_embed: a token id outside [0, N) (reported by bitlin_get_error) */
 } bitlin_status;
 
 #define BITLIN_PERM_NONE 0
@@ -152,6 +153,61 @@ bitlin_status bitlin_forward_host(bitlin_t h, const float* x_host, int M, float*
 bitlin_status bitlin_forward_noalloc(bitlin_t h, const float* x, int M, float* y,
                                      bitlin_stream_t stream);
 
+/*
+ * The MLP block of the model around two folded matrices:
+ *
+ *   y = down( silu(g) * u ),  [g | u] = gate_up(x),  silu(g) = g / (1 + e^-g),
+ *
+ * where gate_up is a handle of 2F rows (rows 0..F-1 the gate matrix, rows
+ * F..2F-1 the up matrix, both over the K of x) and down a handle with K = F.
+ * Each product is the folded product of bitlin_forward (its own signs,
+ * transform and, if set, permutation); SiLU and the product with up are done
+ * in f32 inside the down projection's input gather (decode prologue or
+ * rotation kernel), so the F-wide middle vector is never stored.
+ * Source: "Inside the One-Bit Engine", MLP station (gate and up widen 5120
+ * to 17408; SiLU(gate) multiplies up elementwise, in 32-bit arithmetic; a
+ * third matrix narrows 17408 back to 5120); the Pulse "ARCHITECTURE-SPEC"
+ * page's folded-weights table (ffn_gate, ffn_up and ffn_down carry signs +
+ * WHT).
+ *
+ *   x       device pointer, float [M][gate_up's K], read only.
+ *   y       device pointer, float [M][down's N], fully overwritten.
+ *
+ * Paths and tolerances as bitlin_forward, chosen per handle.  The first call
+ * with a new largest M allocates the [M][2F] gate|up buffer on `down`.
+ * Errors: BITLIN_EINVAL (NULL argument, M < 1, gate_up's N != 2 * down's K,
+ * handles on different devices), BITLIN_ENOMEM, BITLIN_ECUDA, and either
+ * handle's sticky error.
+ */
+bitlin_status bitlin_mlp_forward(bitlin_t gate_up, bitlin_t down, const float* x, int M, float* y,
+                                 bitlin_stream_t stream);
+
+/*
+ * Embedding lookup with the inverse rotation, on the same handle (an N x K
+ * folded matrix whose rows are embeddings):
+ *
+ *   out[m][k] = signs[k] * xt[k],  xt = blockwise normalized Walsh-Hadamard
+ *   transform (blocks of 1024, 1/32) of z, z[k] = (bit(t, k) ? +1 : -1) *
+ *   scale[t][k >> 7], t = ids[m].
+ *
+ * Source: the Pulse "ARCHITECTURE-SPEC" page, Hadamard-fold section: the
+ * embedding lookup takes the transform first and the signs second (h =
+ * signs * WHT(z)), the inverse order of the activation rotation, with the
+ * same normalization and blocks; the row format is the Q1G128 format of the
+ * "Inside the One-Bit Engine" page (station on the embedding row).  The
+ * handle's permutation flag does not apply here.
+ *
+ *   ids     device pointer, int32 [M], token ids.
+ *   out     device pointer, float [M][K], row-major, fully overwritten.
+ *   stream  CUDA stream the work is queued on.
+ *
+ * Asynchronous; allocates nothing.  An id outside [0, N) gives a zero row and
+ * makes the next bitlin_get_error return BITLIN_EINDEX (once; not sticky).
+ * Errors: BITLIN_EINVAL (NULL handle/ids/out, M < 1), BITLIN_ECUDA, and the
+ * handle's sticky error.
+ */
+bitlin_status bitlin_embed(bitlin_t h, const int32_t* ids, int M, float* out, bitlin_stream_t stream);
+
 /* Size in bytes of the fixed scratch array used by bitlin_forward_noalloc. */
 size_t bitlin_noalloc_scratch_bytes(void);
 
@@ -176,8 +232,9 @@ bitlin_status bitlin_destroy(bitlin_t h);
 
 /*
  * Wait for the handle's queued work and report a device-side failure
- * recorded by its kernels (BITLIN_ETIMEOUT when a bounded wait gave up), or
- * BITLIN_ECUDA if synchronizing failed.  The error stays set (sticky).
+ * recorded by its kernels: BITLIN_ETIMEOUT when a bounded wait gave up (stays
+ * set: sticky), BITLIN_EINDEX when bitlin_embed met a token id outside [0, N)
+ * (reported once, then cleared), or BITLIN_ECUDA if synchronizing failed.
  */
 bitlin_status bitlin_get_error(bitlin_t h);
 

@@ -57,6 +57,8 @@ def _load():
     lib.oracle_permute_tiled_to_grouped.argtypes = [P, P]
     lib.oracle_rotate.argtypes = [P, i32, P, i32, P]
     lib.oracle_rotate.restype = i32
+    lib.oracle_rotate_f64.argtypes = [P, i32, P, i32, P]
+    lib.oracle_rotate_f64.restype = i32
     lib.oracle_inverse_rotate.argtypes = [P, i32, P, P]
     lib.oracle_rotate_tokens.argtypes = [P, i32, i32, P, i32, i32, P]
     lib.oracle_rotate_tokens.restype = i32
@@ -150,6 +152,43 @@ def dequant_row(bits: np.ndarray, scales: np.ndarray, n: int) -> np.ndarray:
     out = np.empty(K, dtype=np.float64)
     _load().oracle_dequant_row(_ptr(bits), _ptr(scales), K, int(n), _ptr(out))
     return out
+
+
+def silu(g: np.ndarray) -> np.ndarray:
+    """SiLU(g) = g / (1 + e^-g), f64 ("Inside the One-Bit Engine", MLP station)."""
+    g = np.asarray(g, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g))
+
+
+def rotate_f64(x: np.ndarray, signs: np.ndarray, perm: int) -> np.ndarray:
+    """As rotate, for f64 activations (no rounding of the input to f32)."""
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float64)
+    signs = np.ascontiguousarray(signs, dtype=np.float32)
+    M, K = x.shape
+    out = np.empty((M, K), dtype=np.float64)
+    L = _load()
+    for m in range(M):
+        if L.oracle_rotate_f64(_ptr(x[m]), K, _ptr(signs), int(perm), _ptr(out[m])) != 0:
+            raise MemoryError("oracle rotate: allocation failed")
+    return out
+
+
+def mlp(gu, down, x, rows=None) -> np.ndarray:
+    """The MLP block in f64: [g | u] = forward(gate_up, x) (first F rows gate, next F up),
+    mid = silu(g) * u, y = the folded product of down on mid (kept in f64).  gu and down are
+    (bits, scales, signs, perm)."""
+    F = gu[0].shape[0] // 2
+    h = forward(*gu, x)
+    mid = silu(h[:, :F]) * h[:, F:]
+    bits, scales, signs, perm = down
+    return product(bits, scales, rotate_f64(mid, signs, perm), rows)
+
+
+def embed(bits: np.ndarray, scales: np.ndarray, signs: np.ndarray, ids) -> np.ndarray:
+    """Embedding lookup with the inverse rotation, f64: row ids[m] dequantized, then
+    h = signs * WHT(z) (Pulse "ARCHITECTURE-SPEC", Hadamard-fold section, embedding order)."""
+    return np.stack([inverse_rotate(dequant_row(bits, scales, int(t)), signs) for t in ids])
 
 
 def max_threads() -> int:

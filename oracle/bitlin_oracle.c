@@ -102,8 +102,10 @@ void oracle_permute_tiled_to_grouped(const double* in, double* out)
 
 /* Activation transform applied right before the folded matmul, one token:
  * [permutation if perm] -> times signs -> blockwise normalized transform.
+ * x is f64 here (the MLP block feeds it the f64 middle vector); oracle_rotate
+ * below is the same for f32 activations.
  * Returns 0, or -1 if scratch memory could not be allocated. */
-int oracle_rotate(const float* x, int K, const float* signs, int perm, double* xt)
+int oracle_rotate_f64(const double* x, int K, const float* signs, int perm, double* xt)
 {
     double* t = (double*)malloc(sizeof(double) * (size_t)K);
     double* p = (double*)malloc(sizeof(double) * (size_t)K);
@@ -113,7 +115,7 @@ int oracle_rotate(const float* x, int K, const float* signs, int perm, double* x
         return -1;
     }
     for (int i = 0; i < K; ++i)
-        t[i] = (double)x[i];
+        t[i] = x[i];
     if (perm) {
         oracle_permute_tiled_to_grouped(t, p);
         for (int i = 0; i < K; ++i)
@@ -126,6 +128,18 @@ int oracle_rotate(const float* x, int K, const float* signs, int perm, double* x
     free(t);
     free(p);
     return 0;
+}
+
+int oracle_rotate(const float* x, int K, const float* signs, int perm, double* xt)
+{
+    double* t = (double*)malloc(sizeof(double) * (size_t)K);
+    if (!t)
+        return -1;
+    for (int i = 0; i < K; ++i)
+        t[i] = (double)x[i];
+    int rc = oracle_rotate_f64(t, K, signs, perm, xt);
+    free(t);
+    return rc;
 }
 
 /* The embedding's inverse order: h = signs * WHT(z). */

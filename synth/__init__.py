@@ -15,8 +15,12 @@ a stream be drawn without drawing what precedes it.
 
 Workload shapes follow the Bonsai-27B (qwen35 hybrid) matrices described on
 the "Inside the One-Bit Engine" page (station on the MLP: hidden 5120, ffn
-17408) and the Pulse architecture spec (ssm inner 6144; sign widths
-5120/6144/17408).  Distributions: sign bits are fair coins (the engine page's
+17408; the attention station's projection table: q [12288, 5120] holding
+queries and the output gate, k and v [1024, 5120], o [5120, 6144]) and the
+Pulse architecture spec (ssm inner 6144; the folded-weights table: attn_qkv,
+ssm_out, attn_output; sign widths 5120/6144/17408).  The gated-delta qkv
+(16 key heads x 128 x 2 + 48 value heads x 128 = 10240 rows) and its output
+gate (48 x 128 = 6144 rows) follow from the head counts on the same pages.  Distributions: sign bits are fair coins (the engine page's
 weight forensics measured per-group popcount variance 31.985 against the
 fair-coin 32.0); scales are uniform on a stated interval and rounded to fp16;
 activations are standard normal.
@@ -130,6 +134,12 @@ def workload(name: str, M: int | None = None) -> Workload:
         "gate_up": (1, 5120, 34816, 0.005, 0.03, 0, 5),
         "prefill": (1024, 5120, 17408, 0.005, 0.03, 0, 6),
         "attn_output": (1, 6144, 5120, 0.005, 0.03, 0, 7),
+        # attention-side folded matrices (gated-delta qkv and output gate, full
+        # attention's q-with-gate and k/v projections)
+        "attn_qkv": (1, 5120, 10240, 0.005, 0.03, 0, 8),
+        "attn_gate": (1, 5120, 6144, 0.005, 0.03, 0, 9),
+        "attn_q": (1, 5120, 12288, 0.005, 0.03, 0, 10),
+        "attn_kv": (1, 5120, 1024, 0.005, 0.03, 0, 11),
     }
     m, K, N, lo, hi, perm, cid = table[name]
     if M is not None:

@@ -25,8 +25,8 @@ def test_every_header_function_is_exported(L):
 
 
 def test_status_strings(L):
-    for st in range(6):
-        assert L.bitlin_status_string(st)
+    for st in range(8):
+        assert L.bitlin_status_string(st) != b"unknown status"
     assert L.bitlin_status_string(99) == b"unknown status"
     assert L.bitlin_version() >= 100
 
@@ -47,6 +47,7 @@ def test_argument_validation_without_device(L):
     assert h.value is None
     assert L.bitlin_forward(None, p, 1, p, None) == hrb.BITLIN_EINVAL
     assert L.bitlin_forward_host(None, p, 1, p, None) == hrb.BITLIN_EINVAL
+    assert L.bitlin_embed(None, p, 1, p, None) == hrb.BITLIN_EINVAL
     assert L.bitlin_set_path(None, 0) == hrb.BITLIN_EINVAL
     assert L.bitlin_get_error(None) == hrb.BITLIN_EINVAL
     assert L.bitlin_destroy(None) == hrb.BITLIN_OK

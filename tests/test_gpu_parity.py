@@ -77,7 +77,8 @@ def test_tiny_probe(hrb):
     assert max_rel_l2(y, golden[None, :]) <= DECODE_TOL
 
 
-@pytest.mark.parametrize("name", ["ffn_gate", "ffn_down", "ssm_out", "attn_output"])
+@pytest.mark.parametrize("name", ["ffn_gate", "ffn_down", "ssm_out", "attn_output", "attn_qkv", "attn_gate",
+                                  "attn_q", "attn_kv"])
 def test_decode_full_size_every_output(hrb, name):
     w, bits, scales, signs, x = inputs(name)
     y = run(make_layer(hrb, bits, scales, signs, w.perm), x)
@@ -102,6 +103,17 @@ def test_gate_up_decode_sweep(hrb, M):
     ref = oracle.forward(bits, scales, signs, w.perm, x, rows)
     got = y if rows is None else y[:, rows]
     assert max_rel_l2(got, ref) <= DECODE_TOL
+
+
+@pytest.mark.parametrize("name,M", [("attn_qkv", 4), ("attn_gate", 16), ("attn_q", 8), ("attn_kv", 3),
+                                    ("attn_output", 5)])
+def test_attention_shapes_small_batch(hrb, name, M):
+    """The attention-side folded shapes at 2 <= M < 64 (exact tensor path), sampled rows."""
+    w, bits, scales, signs, x = inputs(name, M)
+    y = run(make_layer(hrb, bits, scales, signs, w.perm), x)
+    rows = synth.sample_rows(w.seed, w.N, 768)
+    ref = oracle.forward(bits, scales, signs, w.perm, x, rows)
+    assert max_rel_l2(y[:, rows], ref) <= DECODE_TOL
 
 
 def test_gate_up_m64_both_paths(hrb):
@@ -263,6 +275,98 @@ def test_auto_path_choice(hrb):
     for m, tol in ((1, DECODE_TOL), (2, DECODE_TOL), (63, DECODE_TOL), (64, PREFILL_TOL), (70, PREFILL_TOL)):
         y = run(layer, np.ascontiguousarray(x[:m]))
         assert max_rel_l2(y[:, rows], ref[:m]) <= tol, m
+
+
+# ------------------------------------------------------------------ MLP block (gate|up -> SiLU -> down)
+
+def _mlp_pair(hrb, F, H, seed):
+    gu = (synth.random_bits(seed, 2 * F, H), synth.random_scales(seed, 2 * F, H, 0.005, 0.03),
+          synth.random_signs(seed, H), 0)
+    dn = (synth.random_bits(seed + 1, H, F), synth.random_scales(seed + 1, H, F, 0.005, 0.03),
+          synth.random_signs(seed + 1, F), 0)
+    return gu, dn, make_layer(hrb, *gu), make_layer(hrb, *dn)
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_mlp_block_full_size(hrb, M):
+    """Bonsai-27B MLP shapes (5120 -> 2 x 17408 -> 5120): M = 1 on the decode GEMVs, M = 4 on
+    the exact tensor path, every output, <= 1e-5."""
+    gu, dn, lgu, ldn = _mlp_pair(hrb, 17408, 5120, 0xB1711A00 + 5)
+    x = synth.random_x(0xB1711A00 + 5, M, 5120)
+    y = hrb.mlp_forward(lgu, ldn, torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    assert lgu.get_error() == 0 and ldn.get_error() == 0
+    ref = oracle.mlp(gu, dn, x)
+    assert max_rel_l2(y.cpu().numpy().astype(np.float64), ref) <= DECODE_TOL
+
+
+def test_mlp_block_bf16_path_and_forced_paths(hrb):
+    """M = 64 runs both products on the bf16 tensor path (<= 1e-2); forcing the f32 decode
+    GEMV on both handles gives <= 1e-5 at the same M."""
+    gu, dn, lgu, ldn = _mlp_pair(hrb, 2048, 1024, 31)
+    x = synth.random_x(32, 64, 1024)
+    ref = oracle.mlp(gu, dn, x)
+    y = hrb.mlp_forward(lgu, ldn, torch.from_numpy(x).cuda())
+    assert max_rel_l2(y.cpu().numpy().astype(np.float64), ref) <= PREFILL_TOL
+    lgu.set_path(hrb.PATH_DECODE)
+    ldn.set_path(hrb.PATH_DECODE)
+    y = hrb.mlp_forward(lgu, ldn, torch.from_numpy(x).cuda())
+    assert max_rel_l2(y.cpu().numpy().astype(np.float64), ref) <= DECODE_TOL
+
+
+def test_mlp_block_rejects_mismatched_pair(hrb):
+    gu, dn, lgu, ldn = _mlp_pair(hrb, 1024, 1024, 41)
+    w, bits, scales, signs, _ = inputs("tiny")
+    other = make_layer(hrb, bits, scales, signs, 0)
+    x = torch.zeros((1, 1024), dtype=torch.float32, device="cuda")
+    with pytest.raises(hrb.BitlinError) as e:
+        hrb.mlp_forward(other, ldn, x)  # other has N = 256, not 2 * 1024
+    assert e.value.status == hrb.BITLIN_EINVAL
+
+
+# ------------------------------------------------------------------ embedding (inverse rotation)
+
+@pytest.mark.parametrize("name,ids", [("tiny", [0, 255, 17, 17, 128]), ("ffn_down", [0, 5119, 1234]),
+                                      ("attn_kv", list(range(0, 1024, 97)) + [1023])])
+def test_embedding_inverse_rotation(hrb, name, ids):
+    """out[m] = signs * WHT(dequantized row ids[m]) against the oracle (f64), <= 1e-5."""
+    w, bits, scales, signs, _ = inputs(name)
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    tid = torch.tensor(ids, dtype=torch.int32, device="cuda")
+    out = layer.embed(tid)
+    torch.cuda.synchronize()
+    assert layer.get_error() == 0
+    ref = oracle.embed(bits, scales, signs, ids)
+    assert max_rel_l2(out.cpu().numpy().astype(np.float64), ref) <= DECODE_TOL
+
+
+def test_embedding_round_trips_through_the_activation_rotation(hrb):
+    """Reading an embedded row back through the activation rotation (signs, then the
+    transform) gives the dequantized row again: the fold's two orders are inverses."""
+    w, bits, scales, signs, _ = inputs("ffn_gate")
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    ids = [3, 17000]
+    h = layer.embed(torch.tensor(ids, dtype=torch.int32, device="cuda")).cpu().numpy().astype(np.float64)
+    for m, t in enumerate(ids):
+        back = oracle.rotate(h[m:m + 1], signs, 0)[0]
+        z = oracle.dequant_row(bits, scales, t)
+        assert np.linalg.norm(back - z) <= 1e-5 * np.linalg.norm(z)
+
+
+def test_embedding_bad_id_reports_once(hrb):
+    w, bits, scales, signs, _ = inputs("tiny")
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    out = layer.embed(torch.tensor([1, 256, -1, 2], dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert layer.get_error() == hrb.BITLIN_EINDEX
+    assert layer.get_error() == 0  # reported once, not sticky
+    o = out.cpu().numpy()
+    assert not o[1].any() and not o[2].any()
+    ref = oracle.embed(bits, scales, signs, [1, 2])
+    assert max_rel_l2(o[[0, 3]].astype(np.float64), ref) <= DECODE_TOL
+    # the handle still works
+    x = synth.random_x(5, 1, w.K)
+    assert max_rel_l2(run(layer, x), oracle.forward(bits, scales, signs, 0, x)) <= DECODE_TOL
 
 
 # ------------------------------------------------------------------ errors

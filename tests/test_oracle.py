@@ -263,3 +263,68 @@ def test_generator_counter_mode_slices_agree():
     a = synth.stream(5, 1, 1000)
     b = synth.stream(5, 1, 300, start=700)
     np.testing.assert_array_equal(a[700:], b)
+
+
+# ------------------------------------------------------------------ NEXT rows: SiLU, MLP block, embedding
+
+def test_silu_against_scipy_expit_and_identities(oracle_lib):
+    """SiLU(g) = g / (1 + e^-g) ("Inside the One-Bit Engine", MLP station) against
+    scipy.special.expit (the logistic function, a library routine) times g, and the
+    identities silu(0) = 0, silu(g) - silu(-g) = g, silu(g) -> g for large g."""
+    import scipy.special
+
+    g = np.concatenate([np.linspace(-30, 30, 1201), [-700.0, 700.0, 0.0]])
+    got = oracle_lib.silu(g)
+    np.testing.assert_allclose(got, g * scipy.special.expit(g), rtol=1e-14, atol=1e-300)
+    assert oracle_lib.silu(np.array([0.0]))[0] == 0.0
+    np.testing.assert_allclose(got - oracle_lib.silu(-g), g, rtol=1e-13, atol=1e-13)
+    assert oracle_lib.silu(np.array([700.0]))[0] == 700.0
+    assert abs(oracle_lib.silu(np.array([-700.0]))[0]) < 1e-300
+    # the small dip below zero: minimum near g = -1.278, value -0.2785
+    assert abs(oracle_lib.silu(np.array([-1.2784645]))[0] + 0.2784645) < 1e-6
+
+
+def test_mlp_block_against_dense_brute_force(oracle_lib):
+    """down(silu(gate x) * (up x)) with the first F rows of gate_up as gate, built from
+    the dense brute-force product and scipy's logistic function."""
+    import scipy.special
+
+    F, Hd = 1024, 2048
+    sgu, sd = 321, 654
+    gu = (synth.random_bits(sgu, 2 * F, Hd), synth.random_scales(sgu, 2 * F, Hd, 0.005, 0.03),
+          synth.random_signs(sgu, Hd), 0)
+    dn = (synth.random_bits(sd, 6, F), synth.random_scales(sd, 6, F, 0.005, 0.03), synth.random_signs(sd, F), 0)
+    x = synth.random_x(7, 2, Hd)
+    got = oracle_lib.mlp(gu, dn, x)
+    h = _dense_reference(*gu, x)
+    mid = h[:, :F] * scipy.special.expit(h[:, :F]) * h[:, F:]
+    ref = _dense_reference(*dn, mid)
+    np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12)
+    # swapping the roles of gate and up changes the answer (the order is pinned)
+    swapped = (np.concatenate([gu[0][F:], gu[0][:F]]), np.concatenate([gu[1][F:], gu[1][:F]]), gu[2], 0)
+    assert np.linalg.norm(oracle_lib.mlp(swapped, dn, x) - got) > 0.1 * np.linalg.norm(got)
+
+
+def test_embedding_closed_form_and_brute_force(oracle_lib):
+    """h = signs * WHT(z) / 32 per block (Pulse spec, embedding order).  Closed form: an
+    all-ones row with one scale s per block gives 32 s at each block's first position
+    (times its sign) and 0 elsewhere; and against the dense Hadamard matrix product."""
+    import scipy.linalg
+
+    K, N = 2048, 4
+    bits = synth.random_bits(77, N, K)
+    scales = synth.random_scales(77, N, K, 0.01, 0.05)
+    signs = synth.random_signs(77, K)
+    bits[2, :] = 0xFFFFFFFF
+    scales[2, :] = np.float16(0.03125).view(np.uint16)  # one scale for the whole row
+    h = oracle_lib.embed(bits, scales, signs, [2])[0]
+    expect = np.zeros(K)
+    expect[0::1024] = 32 * 0.03125
+    np.testing.assert_allclose(h, expect * signs, rtol=0, atol=1e-15)
+    H = scipy.linalg.hadamard(1024).astype(np.float64) / 32.0
+    Hb = np.kron(np.eye(K // 1024), H)
+    pm = np.unpackbits(bits.view(np.uint8), bitorder="little").reshape(N, K).astype(np.float64)
+    Wd = (2 * pm - 1) * np.repeat(scales.view(np.float16).astype(np.float64), 128, axis=1)
+    got = oracle_lib.embed(bits, scales, signs, [0, 3, 1])
+    ref = (Hb @ Wd[[0, 3, 1]].T).T * signs.astype(np.float64)[None, :]
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
