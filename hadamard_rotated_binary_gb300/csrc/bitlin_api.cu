@@ -148,6 +148,7 @@ bitlin_status run_tc(bitlin_t h, const float* x, int M, float* y, cudaStream_t s
     p.M = M;
     p.N = h->N;
     p.K = h->K;
+    p.num_sms = h->num_sms;
     p.wait_budget_ns = h->wait_budget_ns;
     e = exact ? bitlin_launch_tc_exact(p, h->tmap, h->tmap_bits, h->stall_test, s)
               : bitlin_launch_prefill(p, h->tmap, h->tmap_bits, h->stall_test, s);

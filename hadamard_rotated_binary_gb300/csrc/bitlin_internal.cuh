@@ -53,6 +53,7 @@ struct PrefillParams {
     float* y;               // [M][N]
     int* dev_error;
     int M, N, K;
+    int num_sms;            // for the split-K choice
     long long wait_budget_ns;
 };
 

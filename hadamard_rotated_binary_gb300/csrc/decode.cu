@@ -47,6 +47,7 @@
 #include <cuda_fp16.h>
 
 #include "bitlin_internal.cuh"
+#include "ptx.cuh"
 
 namespace {
 
@@ -386,27 +387,6 @@ __device__ __forceinline__ void splitk_finish(const DecodeParams& p, int ta, int
     }
 }
 
-// ---- thread-block cluster (distributed shared memory) helpers --------------
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, int rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ float ld_cluster(uint32_t caddr)
-{
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
-    return v;
-}
-
 // Split-K across a cluster: CTA rank s of the cluster holds slice s's partial
 // sums of the cluster's tiles [ta, tb) in its own shared memory (pbuf,
 // [M][tb - ta][32]).  After a cluster barrier each CTA sums an equal share of
@@ -415,7 +395,7 @@ __device__ __forceinline__ float ld_cluster(uint32_t caddr)
 // keeps every CTA's shared memory alive until the others have read it.
 __device__ __forceinline__ void cluster_finish(const DecodeParams& p, int ta, int tb, int rank, const float* pbuf)
 {
-    cluster_sync();
+    ptx::cluster_sync();
     const int ntile = tb - ta;
     const int rows = p.M * ntile * kTileRows;
     const int lo = (int)((long long)rows * rank / p.S), hi = (int)((long long)rows * (rank + 1) / p.S);
@@ -425,7 +405,7 @@ __device__ __forceinline__ void cluster_finish(const DecodeParams& p, int ta, in
         float v[kMaxClusterSlices];
 #pragma unroll
         for (int j = 0; j < kMaxClusterSlices; ++j)
-            if (j < p.S) v[j] = ld_cluster(cluster_map(a, j));
+            if (j < p.S) v[j] = ptx::ld_cluster(ptx::cluster_map(a, j));
         float sum = 0.f;
 #pragma unroll
         for (int j = 0; j < kMaxClusterSlices; ++j)
@@ -434,7 +414,7 @@ __device__ __forceinline__ void cluster_finish(const DecodeParams& p, int ta, in
         const int n = ta * kTileRows + r;
         if (n < p.N) p.y[(size_t)m * p.N + n] = sum;
     }
-    cluster_sync();
+    ptx::cluster_sync();
 }
 
 __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p)

@@ -61,6 +61,7 @@ constexpr int kBitsBytes = 2048;    // one group's bits: 128 rows x 4 words
 constexpr int kBitsStages = 8;      // bits run this many groups ahead of the expansion
 constexpr int kACols = 64;          // one A stage: 128 lanes x 64 columns (128 bf16 per row)
 constexpr int kTmemCols = 512;      // the whole tensor memory (one CTA per SM)
+constexpr int kMaxSplits = 8;       // split-K clusters along grid.z (portable cluster size)
 
 template <int BN>
 struct Cfg {
@@ -126,7 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kPrefillRows;
     const int b0 = blockIdx.y * BN;  // first B row of this tile
-    const int G = p.K / 128;
+    // Split-K over grid.z: this CTA takes the K-groups [gbase, gbase + G).
+    const int Gall = p.K / 128;
+    const int gbase = (int)((long long)Gall * blockIdx.z / gridDim.z);
+    const int G = (int)((long long)Gall * (blockIdx.z + 1) / gridDim.z) - gbase;
     const long long budget = p.wait_budget_ns;
 
     if (threadIdx.x == 0) {
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st = g % SB;
                 if (g >= SB && !wait_done<R>(bar->done, g - SB, abort, budget)) break;
                 ptx::mbar_arrive_expect_tx(&bar->fullB[st], kBBytes);
-                ptx::tma_load_3d(tileB + st * kBBytes, &tmap_b, 0, b0, 2 * g, &bar->fullB[st]);
+                ptx::tma_load_3d(tileB + st * kBBytes, &tmap_b, 0, b0, 2 * (gbase + g), &bar->fullB[st]);
                 issued = g + 1;
             }
             // Every copy this lane issued must land before the CTA may exit.
@@ -186,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t ph = (uint32_t)(g / kBitsStages) & 1u;
                 if (!ptx::mbar_wait_bounded(&bar->emptyBits[sb], ph ^ 1u, abort, budget)) break;
                 ptx::mbar_arrive_expect_tx(&bar->fullBits[sb], kBitsBytes);
-                ptx::tma_load_2d(tileBits + sb * kBitsBytes, &tmap_bits, g * 4, n0, &bar->fullBits[sb]);
+                ptx::tma_load_2d(tileBits + sb * kBitsBytes, &tmap_bits, (gbase + g) * 4, n0, &bar->fullBits[sb]);
                 issued = g + 1;
             }
             for (int g = (issued > kBitsStages ? issued - kBitsStages : 0); g < issued; ++g) {
@@ -272,17 +276,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         float acc[kAcc];
 #pragma unroll
         for (int j = 0; j < kAcc; ++j) acc[j] = 0.f;
-        const uint16_t* srow = p.scales + (size_t)(valid ? n : 0) * G;
-        // The row's scales, requested kSRing groups ahead (G is a multiple of 8).
+        const uint16_t* srow = p.scales + (size_t)(valid ? n : 0) * Gall + gbase;
+        // The row's scales, requested kSRing groups ahead.
         constexpr int kSRing = 4;
         uint16_t sring[kSRing];
 #pragma unroll
-        for (int u = 0; u < kSRing; ++u) sring[u] = valid ? __ldg(srow + u) : (uint16_t)0;
+        for (int u = 0; u < kSRing; ++u) sring[u] = (valid && u < G) ? __ldg(srow + u) : (uint16_t)0;
         bool ok = true;
         for (int g0 = 0; g0 < G && ok; g0 += kSRing) {
 #pragma unroll
             for (int u = 0; u < kSRing; ++u) {
                 const int g = g0 + u;
+                if (g >= G) break;
                 const int buf = g & 1;
                 const uint32_t tph = (uint32_t)(g >> 1) & 1u;
                 const float s = __half2float(__ushort_as_half(sring[u]));
@@ -314,7 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if (ok && valid) {
+        if (gridDim.z > 1) {
+            // Split-K: park the partial results in the B ring (idle now: every
+            // copy into it has landed and every MMA reading it has completed),
+            // column c = half * kAcc + j, row r: pbuf[c * 128 + r].
+            float* pbuf = reinterpret_cast<float*>(tileB);
+#pragma unroll
+            for (int j = 0; j < kAcc; ++j) pbuf[(half * kAcc + j) * kPrefillRows + r] = acc[j];
+        } else if (ok && valid) {
 #pragma unroll
             for (int j = 0; j < kAcc; ++j) {
                 const int m = EXACT ? (b0 + half * kHalf) / 4 + j : b0 + half * kHalf + j;
@@ -325,6 +337,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
+    if (gridDim.z > 1) {
+        // The split-K CTAs of this tile form a cluster along z.  Each sums an
+        // equal share of the tile's outputs over the cluster's partials, in
+        // rank order 0..S-1 (deterministic), through distributed shared
+        // memory, and writes y; the second barrier keeps every CTA's shared
+        // memory alive until the others have read it.
+        static_assert(2 * kAcc * kPrefillRows * 4 <= C::kStagesB * kBBytes, "partials fit the B ring");
+        ptx::cluster_sync();
+        const int S = gridDim.z;
+        const int rank = (int)ptx::cluster_ctarank();
+        constexpr int E = 2 * kAcc * kPrefillRows;
+        const uint32_t base = ptx::smem_u32(tileB);
+        for (int e = E * rank / S + (int)threadIdx.x; e < E * (rank + 1) / S; e += kThreads) {
+            float v[kMaxSplits];
+#pragma unroll
+            for (int j = 0; j < kMaxSplits; ++j)
+                if (j < S) v[j] = ptx::ld_cluster(ptx::cluster_map(base + 4u * (uint32_t)e, j));
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < kMaxSplits; ++j)
+                if (j < S) sum += v[j];
+            const int c = e / kPrefillRows, r = e - c * kPrefillRows;
+            const int m = EXACT ? b0 / 4 + c : b0 + c;
+            const int n = n0 + r;
+            if (m < p.M && n < p.N) p.y[(size_t)m * p.N + n] = sum;
+        }
+        ptx::cluster_sync();
+    }
     if (warp == kMmaWarp) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
@@ -344,10 +384,33 @@ cudaError_t launch(const PrefillParams& p, const void* tmap, const void* tmap_bi
         configured = true;
     }
     const int rows_b = EXACT ? 4 * p.M : p.M;
-    dim3 grid((p.N + kPrefillRows - 1) / kPrefillRows, (rows_b + BN - 1) / BN);
-    bitlin_tc_gemm<BN, EXACT><<<grid, kThreads, smem_bytes<BN>(), s>>>(
-        *static_cast<const CUtensorMap*>(tmap), *static_cast<const CUtensorMap*>(tmap_bits), p, stall_test);
-    return cudaGetLastError();
+    const int gx = (p.N + kPrefillRows - 1) / kPrefillRows, gy = (rows_b + BN - 1) / BN;
+    // Split K when the tiles would fill less than half of the SMs (tall-K,
+    // short-N matrices at small M, e.g. 17408 -> 5120): as many splits as
+    // still fit one wave, at most 8 and at least 8 K-groups each.
+    int splits = 1;
+    const int tiles = gx * gy, Gall = p.K / 128;
+    if (2 * tiles < p.num_sms) {
+        splits = p.num_sms / tiles;
+        if (splits > kMaxSplits) splits = kMaxSplits;
+        if (splits > Gall / 8) splits = Gall / 8;
+        if (splits < 1) splits = 1;
+    }
+    const CUtensorMap tb = *static_cast<const CUtensorMap*>(tmap);
+    const CUtensorMap tbits = *static_cast<const CUtensorMap*>(tmap_bits);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = splits;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gx, gy, splits);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes<BN>();
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = splits > 1 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, bitlin_tc_gemm<BN, EXACT>, tb, tbits, p, stall_test);
 }
 
 }  // namespace
