@@ -42,10 +42,11 @@ def parse():
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ffn_gate")
-    ap.add_argument("--op", choices=["gemv", "mlp", "embed"], default="gemv",
+    ap.add_argument("--op", choices=["gemv", "mlp", "embed", "lmhead"], default="gemv",
                     help="gemv: one folded product per step (the headline); mlp: the MLP block "
                          "(gate+up 5120x34816, SiLU, down 17408x5120) per step; embed: M embedding "
-                         "lookups with the inverse rotation in a 248,320 x 5120 table per step")
+                         "lookups with the inverse rotation in a 248,320 x 5120 table per step; lmhead: "
+                         "the 248,320 x 5120 vocabulary product and the argmax per step")
     ap.add_argument("--M", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
@@ -261,6 +262,7 @@ def run_reference(args, w: synth.Workload):
 
 MLP_METRIC = "MLP block tokens/s and weight GB/s (1-bit WHT-folded gate+up 5120x34816, SiLU, down 17408x5120)"
 EMBED_METRIC = "embedding lookups/s with the inverse rotation (1-bit WHT-folded table 248320x5120)"
+LMHEAD_METRIC = "LM head tokens/s and weight GB/s (1-bit WHT-folded 248320x5120 product + argmax)"
 
 
 def timed_graph(step, stream, steps: int, warmup: int, pg, dev):
@@ -370,6 +372,57 @@ def run_op(args, ws, rank, local, pg):
 
             oracle.build()
             return lambda: oracle.mlp(gu_in[:3] + (0,), dn_in[:3] + (0,), x)
+    elif args.op == "lmhead":
+        N, K = 248320, 5120
+        seed = 0xB1711A00 + 12
+        bits = synth.random_bits(seed, N, K)
+        scales = synth.random_scales(seed, N, K, 0.005, 0.03)
+        signs = synth.random_signs(seed, K)
+        tb = torch.from_numpy(bits.view(np.int32)).to(dev)
+        ts = torch.from_numpy(scales.view(np.int16)).to(dev)
+        tg = torch.from_numpy(signs).to(dev)
+        wbytes = N * K // 8 + 2 * N * (K // 128)
+        R = args.copies if args.copies else max(2, -(-4 * l2 // wbytes))
+        heads = [hrb.BitLinear(tb, ts, tg, 0) for _ in range(R)]
+        del tb, ts, tg
+        x = synth.random_x(seed, M, K)
+        xd = torch.from_numpy(x).to(dev)
+        lg = torch.empty((M, N), dtype=torch.float32, device=dev)
+        idd = torch.empty((M,), dtype=torch.int32, device=dev)
+
+        def step(i):
+            heads[i % R].argmax(xd, logits=lg, ids=idd, stream=stream)
+
+        ms, clocks = timed_graph(step, stream, args.steps, max(args.warmup, R), pg, dev)
+        s_step = ms / 1e3 / args.steps
+        algo = wbytes + 4 * M * K + 4 * M * N + 4 * K + 4 * M
+        if M == 1:
+            roof = {"bound": "hbm", "achieved": algo / s_step / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "kernel": "bitlin_decode_gemv + bitlin_argmax_rows", "bytes_per_launch": algo}
+        else:
+            digits = 3 if M < 64 else 1
+            flops = 2.0 * M * digits * N * K
+            roof = {"bound": "tensor", "achieved": flops / s_step / 1e12, "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "kernel": "bitlin_tc_gemm + bitlin_argmax_rows", "flops_per_launch": flops}
+        roof.update({"frac": roof["achieved"] / roof["peak"], "peak_kind": peak_kind, "traffic": None})
+        metric, config = LMHEAD_METRIC, {"workload": "lm_head", "M": M, "N": N, "K": K, "weight_copies": R,
+                                         "weight_set_bytes": R * wbytes,
+                                         "l2": f"inputs larger than L2: {R} distinct copies cycled"}
+        launches, wgb = (2 if M == 1 else 3), wbytes / s_step / 1e9
+
+        def e2e_call(xh, yh):
+            xd.copy_(xh, non_blocking=True)
+            heads[0].argmax(xd, logits=lg, ids=idd)
+            yh.copy_(idd, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        h2d, d2h = 4 * M * K, 4 * M
+
+        def cpu_call():
+            import oracle
+
+            oracle.build()
+            return lambda: np.argmax(oracle.forward(bits, scales, signs, 0, x), axis=1)
     else:
         N, K = 248320, 5120
         seed = 0xB1711A00 + 12
@@ -414,7 +467,10 @@ def run_op(args, ws, rank, local, pg):
 
     # end to end through the Python API: pinned host input -> device, call, device -> pinned host
     xh = torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
-    yh = torch.empty(out_shape, dtype=torch.float32).pin_memory()
+    if args.op == "lmhead":
+        yh = torch.empty((M,), dtype=torch.int32).pin_memory()
+    else:
+        yh = torch.empty(out_shape, dtype=torch.float32).pin_memory()
     e2e_steps = min(args.steps, args.e2e_steps)
     for _ in range(3):
         e2e_call(xh, yh)

@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
     L.bitlin_noalloc_scratch_bytes.restype = ctypes.c_size_t
     L.bitlin_embed.argtypes = [P, P, i32, P, P]
     L.bitlin_mlp_forward.argtypes = [P, P, P, i32, P, P]
+    L.bitlin_argmax.argtypes = [P, P, i32, P, P, P]
     L.bitlin_set_path.argtypes = [P, i32]
     L.bitlin_set_wait_budget.argtypes = [P, i64]
     L.bitlin_test_stall.argtypes = [P, i32]
@@ -75,7 +76,7 @@ def lib() -> ctypes.CDLL:
     L.bitlin_cuda_error.argtypes = [P]
     L.bitlin_status_string.argtypes = [i32]
     L.bitlin_status_string.restype = ctypes.c_char_p
-    for name in ("bitlin_create", "bitlin_forward", "bitlin_forward_host", "bitlin_embed", "bitlin_mlp_forward", "bitlin_set_path",
+    for name in ("bitlin_create", "bitlin_forward", "bitlin_forward_host", "bitlin_embed", "bitlin_mlp_forward", "bitlin_argmax", "bitlin_set_path",
                  "bitlin_set_wait_budget", "bitlin_test_stall", "bitlin_destroy", "bitlin_get_error",
                  "bitlin_cuda_error", "bitlin_version"):
         getattr(L, name).restype = i32
@@ -177,6 +178,20 @@ class BitLinear:
         self._check(lib().bitlin_forward_noalloc(self._h, x.data_ptr(), M, out.data_ptr(),
                                                  _stream_handle(stream)), "bitlin_forward_noalloc")
         return out
+
+    def argmax(self, x, logits=None, ids=None, stream=None):
+        """bitlin_argmax: int32 [M] ids of the largest score per token (smallest index on ties);
+        the scores go to `logits` ([M][N] float32) when given."""
+        import torch
+
+        if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous() or x.dim() != 2:
+            raise ValueError("x must be a contiguous float32 CUDA tensor [M][K]")
+        M = int(x.shape[0])
+        if ids is None:
+            ids = torch.empty((M,), dtype=torch.int32, device=x.device)
+        self._check(lib().bitlin_argmax(self._h, x.data_ptr(), M, logits.data_ptr() if logits is not None else None,
+                                        ids.data_ptr(), _stream_handle(stream)), "bitlin_argmax")
+        return ids
 
     def embed(self, ids, out=None, stream=None):
         """bitlin_embed: rows ids (int32 CUDA tensor [M]) of the matrix, dequantized and

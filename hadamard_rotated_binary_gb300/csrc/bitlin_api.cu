@@ -47,6 +47,9 @@ void release(bitlin_t h)
     free_dev(h->hx);
     free_dev(h->hy);
     free_dev(h->mlp_in);
+    free_dev(h->logits);
+    free_dev(h->amax_cand);
+    free_dev(h->amax_tickets);
     if (h->h_err) cudaFreeHost(h->h_err);
     h->h_err = nullptr;
 }
@@ -393,6 +396,41 @@ bitlin_status bitlin_get_error(bitlin_t h)
         return BITLIN_EINDEX;
     }
     return h->sticky;
+}
+
+bitlin_status bitlin_argmax(bitlin_t h, const float* x, int M, float* logits, int32_t* ids,
+                            bitlin_stream_t stream)
+{
+    if (!h || !x || !ids || M < 1) return BITLIN_EINVAL;
+    if (h->sticky != BITLIN_OK) return h->sticky;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    float* y = logits;
+    if (!y) {
+        if (!h->logits || h->logits_M < M) {
+            free_dev(h->logits);
+    free_dev(h->amax_cand);
+    free_dev(h->amax_tickets);
+            h->logits_M = 0;
+            cudaError_t e = cudaMalloc(&h->logits, (size_t)M * h->N * sizeof(float));
+            if (e != cudaSuccess) return from_cuda(h, e);
+            h->logits_M = M;
+        }
+        y = h->logits;
+    }
+    if (!h->amax_cand || h->amax_M < M) {
+        free_dev(h->amax_cand);
+        free_dev(h->amax_tickets);
+        h->amax_M = 0;
+        cudaError_t e = cudaMalloc(&h->amax_cand, bitlin_argmax_scratch_bytes(M));
+        if (e == cudaSuccess) e = cudaMalloc(&h->amax_tickets, (size_t)M * sizeof(unsigned));
+        if (e == cudaSuccess) e = cudaMemset(h->amax_tickets, 0, (size_t)M * sizeof(unsigned));
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return from_cuda(h, e);
+        h->amax_M = M;
+    }
+    bitlin_status st = run_path(h, x, M, y, s, 0);
+    if (st != BITLIN_OK) return st;
+    return from_cuda(h, bitlin_launch_argmax(y, M, h->N, h->amax_cand, h->amax_tickets, ids, s));
 }
 
 bitlin_status bitlin_embed(bitlin_t h, const int32_t* ids, int M, float* out, bitlin_stream_t stream)

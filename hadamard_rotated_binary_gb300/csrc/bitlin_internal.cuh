@@ -95,6 +95,12 @@ struct bitlin {
     // up outputs [M][2K] that the down projection reads through SiLU
     float* mlp_in = nullptr;
     int mlp_M = 0;
+    // bitlin_argmax without a caller buffer: the scores [M][N]
+    float* logits = nullptr;
+    int logits_M = 0;
+    void* amax_cand = nullptr;      // per-chunk (value, index) candidates
+    unsigned* amax_tickets = nullptr;  // one per token, zero between calls
+    int amax_M = 0;
 
     // host-buffer entry point staging
     float* hx = nullptr;
@@ -109,6 +115,9 @@ cudaError_t bitlin_launch_repack_prefill(const uint32_t* bits, int N, int K, uin
                                          cudaStream_t s);
 cudaError_t bitlin_launch_check_signs(const float* signs, int K, int* bad, cudaStream_t s);
 cudaError_t bitlin_launch_decode(const bitlin_impl::DecodeParams& p, int num_sms, cudaStream_t s);
+cudaError_t bitlin_launch_argmax(const float* y, int M, int N, void* cand, unsigned* tickets, int32_t* ids,
+                                 cudaStream_t s);
+size_t bitlin_argmax_scratch_bytes(int M);
 cudaError_t bitlin_launch_embed(const uint32_t* bits, const uint16_t* scales, const float* signs,
                                 const int32_t* ids, int M, int N, int K, float* out, int* dev_error,
                                 cudaStream_t s);

@@ -289,6 +289,10 @@ __device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes, int tid
     }
 }
 
+// Units (slice x 32-row tile, 2 KB of bits) a CTA prefetches into L2 before
+// the wait: 64 units = 128 KB, 19.5 MB over 152 CTAs.
+constexpr int kPrefetchUnits = 64;
+
 // Tiles in flight per warp: the register ring of prefetched tiles (even).
 #ifndef BITLIN_DECODE_RING
 #define BITLIN_DECODE_RING 4
@@ -456,10 +460,14 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
     // The weights do not depend on the previous kernel: start streaming this
     // CTA's whole share (one contiguous range of bits and one of scales) from
     // HBM into L2 before waiting for it.
-#ifndef BITLIN_NO_L2_PREFETCH
-    prefetch_l2(p.bits + (size_t)u0 * 128, (size_t)(u1 - u0) * 2048, threadIdx.x);
-    prefetch_l2(p.scales + (size_t)u0 * 32, (size_t)(u1 - u0) * 256, (threadIdx.x + 128) % kDecodeThreads);
-#endif
+    // At most the first kPrefetchUnits units: for matrices larger than L2 (the
+    // 179 MB vocabulary matrix) a prefetch of everything would evict itself
+    // before use; the register ring streams the rest.
+    {
+        const int pu = min(u1 - u0, kPrefetchUnits);
+        prefetch_l2(p.bits + (size_t)u0 * 128, (size_t)pu * 2048, threadIdx.x);
+        prefetch_l2(p.scales + (size_t)u0 * 32, (size_t)pu * 256, (threadIdx.x + 128) % kDecodeThreads);
+    }
     // Before the wait: this warp's first tiles (ta + warp + warps * j, j < kRing) and
     // the signs of the first segment, whose latency then overlaps the wait, and
     // the L2 hint for x.
@@ -549,8 +557,9 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
 
 namespace {
 
-// Cluster launches reserve this much shared memory for the partial sums.
-constexpr int kPbufBytes = 16384;
+// Cluster launches reserve up to this much shared memory for the partial
+// sums (the vocabulary matrix, 248,320 rows over 13 clusters, needs 76 KB).
+constexpr int kPbufBytes = 96 * 1024;
 
 // Clusters of S CTAs that one call may use, by S: the clusters that can be
 // resident at once divided by the CTAs that fit on an SM, so that when two
@@ -613,11 +622,11 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
         if (maxc > 0) {
             const int ncl = maxc < p.T ? maxc : p.T;
             const long long pb = (long long)p.M * ((p.T + ncl - 1) / ncl) * kTileRows * 4;
-            if (pb <= kPbufBytes) {
+            if (pb <= kPbufBytes && kPbufOff + pb <= g_max_smem) {
                 q.cluster = 1;
                 q.ctas_per_slice = ncl;
                 grid = p.S * ncl;
-                smem = kPbufOff + kPbufBytes;
+                smem = kPbufOff + (int)pb;
                 cluster = p.S;
             }
         }

@@ -154,6 +154,27 @@ bitlin_status bitlin_forward_noalloc(bitlin_t h, const float* x, int M, float* y
                                      bitlin_stream_t stream);
 
 /*
+ * Greedy choice after the LM head: the folded product of x (as bitlin_forward:
+ * same paths and tolerances), then ids[m] = the smallest n at which y[m][n] is
+ * largest (a NaN score counts as largest).
+ * Source: "Inside the One-Bit Engine", station on the LM head (the folded
+ * vocabulary matrix, 248,320 x 5,120, gives one score per vocabulary entry)
+ * and the Pulse "ARCHITECTURE-SPEC" folded-weights table (output.weight
+ * carries signs + WHT, verified by argmax match).
+ *
+ *   x       device pointer, float [M][K], read only.
+ *   logits  device pointer, float [M][N], overwritten with the scores, or NULL:
+ *           the handle then keeps the scores in a buffer of its own (allocated
+ *           on the first call with a new largest M).
+ *   ids     device pointer, int32 [M], overwritten.
+ *
+ * Errors: BITLIN_EINVAL (NULL handle/x/ids, M < 1), BITLIN_ENOMEM,
+ * BITLIN_ECUDA, and the handle's sticky error.
+ */
+bitlin_status bitlin_argmax(bitlin_t h, const float* x, int M, float* logits, int32_t* ids,
+                            bitlin_stream_t stream);
+
+/*
  * The MLP block of the model around two folded matrices:
  *
  *   y = down( silu(g) * u ),  [g | u] = gate_up(x),  silu(g) = g / (1 + e^-g),

@@ -140,6 +140,8 @@ def workload(name: str, M: int | None = None) -> Workload:
         "attn_gate": (1, 5120, 6144, 0.005, 0.03, 0, 9),
         "attn_q": (1, 5120, 12288, 0.005, 0.03, 0, 10),
         "attn_kv": (1, 5120, 1024, 0.005, 0.03, 0, 11),
+        # the folded vocabulary matrix (LM head, output.weight)
+        "lm_head": (1, 5120, 248320, 0.005, 0.03, 0, 12),
     }
     m, K, N, lo, hi, perm, cid = table[name]
     if M is not None:

@@ -48,6 +48,8 @@ def test_argument_validation_without_device(L):
     assert L.bitlin_forward(None, p, 1, p, None) == hrb.BITLIN_EINVAL
     assert L.bitlin_forward_host(None, p, 1, p, None) == hrb.BITLIN_EINVAL
     assert L.bitlin_embed(None, p, 1, p, None) == hrb.BITLIN_EINVAL
+    assert L.bitlin_argmax(None, p, 1, None, p, None) == hrb.BITLIN_EINVAL
+    assert L.bitlin_mlp_forward(None, None, p, 1, p, None) == hrb.BITLIN_EINVAL
     assert L.bitlin_set_path(None, 0) == hrb.BITLIN_EINVAL
     assert L.bitlin_get_error(None) == hrb.BITLIN_EINVAL
     assert L.bitlin_destroy(None) == hrb.BITLIN_OK

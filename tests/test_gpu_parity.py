@@ -324,6 +324,54 @@ def test_mlp_block_rejects_mismatched_pair(hrb):
     assert e.value.status == hrb.BITLIN_EINVAL
 
 
+# ------------------------------------------------------------------ LM head + argmax
+
+def _lm_head():
+    N, K, seed = 248320, 5120, 0xB1711A00 + 12
+    return (synth.random_bits(seed, N, K), synth.random_scales(seed, N, K, 0.005, 0.03),
+            synth.random_signs(seed, K), seed)
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_lm_head_argmax_full_size(hrb, M):
+    """The folded vocabulary matrix (248,320 x 5,120): scores within 1e-5 of the oracle; the
+    id is the argmax of the scores the GPU computed (same precision decides), and its oracle
+    score is the oracle's maximum up to that tolerance."""
+    bits, scales, signs, seed = _lm_head()
+    x = synth.random_x(seed, M, 5120)
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    logits = torch.empty((M, bits.shape[0]), dtype=torch.float32, device="cuda")
+    ids = layer.argmax(torch.from_numpy(x).cuda(), logits=logits).cpu().numpy()
+    torch.cuda.synchronize()
+    assert layer.get_error() == 0
+    lg = logits.cpu().numpy()
+    ref = oracle.forward(bits, scales, signs, 0, x)
+    assert max_rel_l2(lg.astype(np.float64), ref) <= DECODE_TOL
+    for m in range(M):
+        assert ids[m] == int(np.argmax(lg[m]))
+        assert ref[m, ids[m]] >= ref[m].max() - DECODE_TOL * np.linalg.norm(ref[m])
+    # without a caller buffer: same ids
+    assert np.array_equal(layer.argmax(torch.from_numpy(x).cuda()).cpu().numpy(), ids)
+
+
+def test_argmax_ties_take_the_smallest_index(hrb):
+    """Rows 100 and 132 (same lane, so the same summation order) are identical and carry the
+    largest scores; zero input makes every score exactly 0."""
+    w, bits, scales, signs, x = inputs("tiny")
+    bits = bits.copy()
+    scales = scales.copy()
+    scales[:] = np.float16(1e-4).view(np.uint16)
+    bits[132] = bits[100]
+    scales[100] = scales[132] = np.float16(0.05).view(np.uint16)
+    if oracle.forward(bits, scales, signs, 0, x, [100])[0, 0] < 0:
+        bits[100] = ~bits[100]
+        bits[132] = bits[100]
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    assert layer.argmax(torch.from_numpy(x).cuda()).cpu().numpy()[0] == 100
+    z = torch.zeros((2, w.K), dtype=torch.float32, device="cuda")
+    assert layer.argmax(z).cpu().numpy().tolist() == [0, 0]
+
+
 # ------------------------------------------------------------------ embedding (inverse rotation)
 
 @pytest.mark.parametrize("name,ids", [("tiny", [0, 255, 17, 17, 128]), ("ffn_down", [0, 5119, 1234]),
