@@ -5,7 +5,7 @@
 // final hidden state into one score per token of the vocabulary; picking one
 // word from the scores starts from the largest.
 //
-// A grid of kChunks CTAs per token, each reducing one contiguous chunk of
+// A grid of 256 CTAs per token, each reducing one contiguous chunk of
 // the row (strided coalesced reads, four loads in flight per thread; the
 // scores were just written and sit in L2) to a (value, index) candidate.
 // The CTA that takes a token's last ticket picks among the candidates and
@@ -26,8 +26,9 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi)
     return i < bi;
 }
 
-constexpr int kChunks = 64;
+constexpr int kChunks = 256;  // one chunk per CTA; the final pick reads one candidate per thread
 constexpr int kThreadsA = 256;
+static_assert(kChunks <= kThreadsA, "the final pick reads one candidate per thread");
 
 __device__ __forceinline__ void warp_best(float& bv, int& bi)
 {
