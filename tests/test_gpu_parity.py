@@ -174,6 +174,35 @@ def test_decode_ragged(hrb, N, K, M):
     assert max_rel_l2(y, ref) <= DECODE_TOL
 
 
+@pytest.mark.parametrize("N,K,M,path", [(300, 65536, 1, "decode"), (257, 65536, 3, "exact"),
+                                         (129, 81920, 1, "decode")])
+def test_maximum_widths(hrb, N, K, M, path):
+    """Wide K: 128 and 160 slices of 512 (more slices than SMs: the decode GEMV splits the units
+    over the grid with the global-scratch split-K), and the exact tensor path over 512 K-groups."""
+    seed = 19 + N + K + M
+    bits = synth.random_bits(seed, N, K)
+    scales = synth.random_scales(seed, N, K, 0.005, 0.03)
+    signs = synth.random_signs(seed, K)
+    x = synth.random_x(seed, M, K)
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    y = run(layer, x, path=hrb.PATH_DECODE if path == "decode" else hrb.PATH_TC_EXACT)
+    ref = oracle.forward(bits, scales, signs, 0, x)
+    assert max_rel_l2(y, ref) <= DECODE_TOL
+
+
+def test_prefill_many_tokens(hrb):
+    """M = 4096 tokens (32 token tiles per weight-row tile) on the bf16 tensor path, sampled rows."""
+    N, K, M = 384, 2048, 4096
+    seed = 91
+    bits = synth.random_bits(seed, N, K)
+    scales = synth.random_scales(seed, N, K, 0.005, 0.03)
+    signs = synth.random_signs(seed, K)
+    x = synth.random_x(seed, M, K)
+    y = run(make_layer(hrb, bits, scales, signs, 0), x)
+    ref = oracle.forward(bits, scales, signs, 0, x)
+    assert max_rel_l2(y, ref) <= PREFILL_TOL
+
+
 def test_prefill_path_forced_at_one_token(hrb):
     w, bits, scales, signs, x = inputs("tiny")
     y = run(make_layer(hrb, bits, scales, signs, 0), x, path=hrb.PATH_PREFILL)
@@ -418,6 +447,23 @@ def test_embedding_bad_id_reports_once(hrb):
 
 
 # ------------------------------------------------------------------ errors
+
+def test_empty_and_mismatched_inputs_are_rejected(hrb):
+    """M = 0 (an empty batch) and wrong shapes are argument errors, reported before any launch."""
+    w, bits, scales, signs, x = inputs("tiny")
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    empty = torch.empty((0, w.K), dtype=torch.float32, device="cuda")
+    with pytest.raises(hrb.BitlinError) as e:
+        layer(empty, out=torch.empty((0, w.N), dtype=torch.float32, device="cuda"))
+    assert e.value.status == hrb.BITLIN_EINVAL
+    with pytest.raises(hrb.BitlinError) as e:
+        layer.embed(torch.empty((0,), dtype=torch.int32, device="cuda"), out=torch.empty((0, w.K), device="cuda"))
+    assert e.value.status == hrb.BITLIN_EINVAL
+    with pytest.raises(ValueError):
+        layer(torch.zeros((1, w.K + 32), dtype=torch.float32, device="cuda"))
+    # the handle is unaffected
+    assert max_rel_l2(run(layer, x), oracle.forward(bits, scales, signs, 0, x)) <= DECODE_TOL
+
 
 def test_signs_must_be_plus_minus_one(hrb):
     w, bits, scales, signs, x = inputs("tiny")
