@@ -48,6 +48,8 @@ def parse():
                          "lookups with the inverse rotation in a 248,320 x 5120 table per step; lmhead: "
                          "the 248,320 x 5120 vocabulary product and the argmax per step")
     ap.add_argument("--M", type=int, default=None)
+    ap.add_argument("--path", choices=["auto", "decode", "prefill", "exact"], default="auto",
+                    help="force the library's path (bitlin_set_path) instead of its choice by M")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
     ap.add_argument("--e2e-steps", type=int, default=20000)
@@ -158,24 +160,29 @@ def max_over_ranks(v: float, pg, device) -> float:
     return float(t.item())
 
 
-def path_of(w: synth.Workload) -> str:
-    """Kernel that does the bulk of one call: the decode GEMV (M = 1) or the tcgen05 GEMM."""
-    return "bitlin_decode_gemv" if w.M == 1 else "bitlin_tc_gemm"
+def uses_decode(w: synth.Workload, path: str = "auto") -> bool:
+    """Whether the library runs the decode GEMV for this call (its own choice: M <= 4)."""
+    return path == "decode" or (path == "auto" and w.M <= 4)
 
 
-def roofline(w: synth.Workload, s_per_step: float, peaks: dict, peak_kind: str) -> dict:
+def path_of(w: synth.Workload, path: str = "auto") -> str:
+    """Kernel that does the bulk of one call: the decode GEMV or the tcgen05 GEMM."""
+    return "bitlin_decode_gemv" if uses_decode(w, path) else "bitlin_tc_gemm"
+
+
+def roofline(w: synth.Workload, s_per_step: float, peaks: dict, peak_kind: str, path: str = "auto") -> dict:
     """Roofline of the dominant kernel.  M = 1: HBM-bound, algorithmic bytes per launch over the
     launch time (one launch per step).  M >= 2: the tensor-core GEMM, 2*M*N*K bf16 MMA flops per
     launch (the exact path multiplies three bf16 digit columns per token, 3x that) over the step
     time, which also holds the small rotation kernel, so the fraction is a lower bound; peak = the
     measured burst bf16 GEMM rate (the timed loop lasts milliseconds)."""
-    kernel = path_of(w)
-    if w.M == 1:
+    kernel = path_of(w, path)
+    if uses_decode(w, path):
         achieved = w.algorithmic_bytes() / s_per_step / 1e9
         return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_kind": peak_kind, "kernel": kernel,
                 "bytes_per_launch": w.algorithmic_bytes(), "traffic": traffic_record(kernel, w.name)}
-    digits = 3 if w.M < 64 else 1
+    digits = 3 if (path == "exact" or (path == "auto" and w.M < 64)) else 1
     flops = 2.0 * w.M * digits * w.N * w.K
     achieved = flops / s_per_step / 1e12
     return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -546,6 +553,10 @@ def main():
     R = args.copies if args.copies else max(2, -(-4 * l2 // wbytes))
     layers = [hrb.BitLinear(tb, ts, tg, w.perm) for _ in range(R)]
     del tb, ts, tg
+    forced = {"auto": hrb.PATH_AUTO, "decode": hrb.PATH_DECODE, "prefill": hrb.PATH_PREFILL,
+              "exact": hrb.PATH_TC_EXACT}[args.path]
+    for layer in layers:
+        layer.set_path(forced)
     xd = torch.from_numpy(x).to(dev)
     yd = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
 
@@ -632,14 +643,14 @@ def main():
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded SplitMix64: Bernoulli(0.5) bits, U[0.005,0.03] fp16 scales, +-1 signs, N(0,1) x)",
-        "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "perm": w.perm,
+        "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "perm": w.perm, "path": args.path,
                    "weight_copies": R, "weight_set_bytes": R * wbytes,
                    "l2": f"inputs larger than L2: {R} distinct weight copies ({R * wbytes / 1e6:.0f} MB) cycled",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "weight_gbs": w.weight_bytes() / s_per_step / 1e9,
         "hbm_frac_of_8tbs": achieved / 8000.0,
-        "roofline": roofline(w, s_per_step, peaks, peak_kind),
-        "gpu_launches": args.steps * (1 if w.M == 1 else 2),  # M = 1: one GEMV; else rotate + GEMM
+        "roofline": roofline(w, s_per_step, peaks, peak_kind, args.path),
+        "gpu_launches": args.steps * (1 if uses_decode(w, args.path) else 2),  # GEMV; or rotate + GEMM
         "clocks": clocks,
         "e2e": {"value": ws * w.M * e2e_steps / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": 4 * w.M * w.K, "d2h_bytes_per_step": 4 * w.M * w.N,

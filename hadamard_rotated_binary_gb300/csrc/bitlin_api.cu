@@ -312,7 +312,7 @@ namespace {
 int choose_path(bitlin_t h, int M)
 {
     if (h->path != BITLIN_PATH_AUTO) return h->path;
-    return M >= kPrefillMinM ? BITLIN_PATH_PREFILL : M >= 2 ? BITLIN_PATH_TC_EXACT : BITLIN_PATH_DECODE;
+    return M >= kPrefillMinM ? BITLIN_PATH_PREFILL : M > kDecodeMaxM ? BITLIN_PATH_TC_EXACT : BITLIN_PATH_DECODE;
 }
 
 bitlin_status run_path(bitlin_t h, const float* x, int M, float* y, cudaStream_t s, int swiglu)

@@ -26,7 +26,11 @@ constexpr int kTicketStride = 32;     // one split-K ticket per 128-byte line
 // ---- prefill layout ------------------------------------------------------
 constexpr int kPrefillRows = 128;     // weight rows per CTA (UMMA M)
 constexpr int kPrefillTokens = 128;   // tokens per CTA (UMMA N)
-constexpr int kPrefillMinM = 64;      // auto path switch
+constexpr int kPrefillMinM = 64;      // auto path: bf16 tensor path from this M
+// Auto path: the decode GEMV up to this M (tokens one after the other, each
+// with its own tables; measured faster than the exact tensor path up to 2-4
+// tokens, e.g. gate_up 5120 x 34816 at M = 4: 33 us against 55 us).
+constexpr int kDecodeMaxM = 4;
 
 // Device-side error word values (bitlin_t::dev_error).
 constexpr int kDevErrTimeout = 1;

@@ -296,12 +296,13 @@ def test_tc_exact_path_every_tile_width(hrb, M, N, K, perm):
 
 
 def test_auto_path_choice(hrb):
-    """M = 1 -> table GEMV, 2..63 -> exact tensor path, >= 64 -> bf16 tensor path; all in tolerance."""
+    """M <= 4 -> table GEMV, 5..63 -> exact tensor path, >= 64 -> bf16 tensor path; all in tolerance."""
     w, bits, scales, signs, x = inputs("ffn_gate", 70)
     layer = make_layer(hrb, bits, scales, signs, 0)
     rows = synth.sample_rows(w.seed, w.N, 256)
     ref = oracle.forward(bits, scales, signs, 0, x, rows)
-    for m, tol in ((1, DECODE_TOL), (2, DECODE_TOL), (63, DECODE_TOL), (64, PREFILL_TOL), (70, PREFILL_TOL)):
+    for m, tol in ((1, DECODE_TOL), (2, DECODE_TOL), (4, DECODE_TOL), (5, DECODE_TOL), (63, DECODE_TOL),
+                   (64, PREFILL_TOL), (70, PREFILL_TOL)):
         y = run(layer, np.ascontiguousarray(x[:m]))
         assert max_rel_l2(y[:, rows], ref[:m]) <= tol, m
 
