@@ -58,8 +58,11 @@ constexpr int kSmemTranspose = 16 * kPad * 4;           // 2112 B
 constexpr int kSmemSlice = (kSlice + kSlice / 32) * 4;  // 528 floats
 constexpr int kMaxList = 1024;                          // finished-tile list (ints)
 constexpr int kDecodeSmem = kLutBytes + kSmemTranspose + kSmemSlice + (kMaxList + 1) * 4;
-// Cluster split-K: the CTA's partial sums [M][tiles][32] follow, 16-byte aligned.
-constexpr int kPbufOff = (kDecodeSmem + 15) & ~15;
+// With M >= 2 a second 64 KB table follows (tokens are taken two at a time),
+// then, for the cluster split-K, the CTA's partial sums [M][tiles][32].
+constexpr int kLut2Off = (kDecodeSmem + 127) & ~127;
+constexpr int kPbufOff = (kDecodeSmem + 15) & ~15;  // M = 1
+constexpr int kPbufOff2 = kLut2Off + kLutBytes;     // M >= 2
 constexpr int kMaxClusterSlices = 16;
 constexpr int kRowsPerWarp = 16 / kDecodeWarps;  // rows of the [16][32] transform view per warp
 static_assert(kDecodeWarps == 8 || kDecodeWarps == 16, "prologue mapping assumes 8 or 16 warps");
@@ -277,6 +280,41 @@ __device__ __forceinline__ void tile_dot2(const unsigned char* lut, const uint4 
     out1 = acc1;
 }
 
+// One tile against two tokens' tables: every byte's shared-memory offset is
+// built once and read in both tables (the second at lut2), so each loaded
+// weight tile serves two tokens.
+__device__ __forceinline__ void tile_dot_two(const unsigned char* lut, const unsigned char* lut2,
+                                             const uint4 (&b)[4], uint2 sc, uint32_t base_off, float& out0,
+                                             float& out1)
+{
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const uint32_t w[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+        float g0 = 0.f, g1 = 0.f, h0 = 0.f, h1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t pos = 4u * u + c;
+            const uint32_t off = base_off ^ ((4u * pos) * 0x101u);
+            const uint32_t o0 = __byte_perm(w[c], off, 0x7604), o1 = __byte_perm(w[c], off, 0x7615);
+            const uint32_t o2 = __byte_perm(w[c], off, 0x7624), o3 = __byte_perm(w[c], off, 0x7635);
+            g0 += lut_at(lut, o0);
+            h0 += lut_at(lut2, o0);
+            g1 += lut_at(lut, o1);
+            h1 += lut_at(lut2, o1);
+            g0 += lut_at(lut + 128, o2);
+            h0 += lut_at(lut2 + 128, o2);
+            g1 += lut_at(lut + 128, o3);
+            h1 += lut_at(lut2 + 128, o3);
+        }
+        const float sv = __half2float(__ushort_as_half((unsigned short)((u < 2 ? sc.x : sc.y) >> (16 * (u & 1)))));
+        acc0 = fmaf(g0 + g1, sv, acc0);
+        acc1 = fmaf(h0 + h1, sv, acc1);
+    }
+    out0 = acc0;
+    out1 = acc1;
+}
+
 // Ask L2 to fetch [p, p + bytes) from HBM (no completion tracking), in 16 KB
 // pieces spread over the CTA's threads so that no warp spends long issuing.
 __device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes, int tid)
@@ -421,15 +459,21 @@ __device__ __forceinline__ void cluster_finish(const DecodeParams& p, int ta, in
     ptx::cluster_sync();
 }
 
+// TWO: tokens are taken two at a time (M >= 2), with a 2-deep register ring so
+// that both tokens' accumulators fit the register budget; M = 1 keeps the
+// 4-deep ring.
+template <bool TWO>
 __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p)
 {
+    constexpr int RING = TWO ? 2 : kRing;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* lut = smem;
     float* tbuf = reinterpret_cast<float*>(smem + kLutBytes);
     float* xs = tbuf + 16 * kPad;
     int* done_list = reinterpret_cast<int*>(xs + kSlice + kSlice / 32);  // [kMaxList]
     int* done_count = done_list + kMaxList;
-    float* pbuf = reinterpret_cast<float*>(smem + kPbufOff);  // cluster split-K only
+    unsigned char* lut2 = smem + kLut2Off;  // second token's table (M >= 2)
+    float* pbuf = reinterpret_cast<float*>(smem + (p.M >= 2 ? kPbufOff2 : kPbufOff));  // cluster split-K only
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Units owned by this CTA, [u0, u1) in slice-major order.  With
@@ -471,13 +515,13 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
     // Before the wait: this warp's first tiles (ta + warp + warps * j, j < kRing) and
     // the signs of the first segment, whose latency then overlaps the wait, and
     // the L2 hint for x.
-    uint4 rb[kRing][4];
-    uint2 rs[kRing];
+    uint4 rb[RING][4];
+    uint2 rs[RING];
     float xv[4 * kRowsPerWarp];
     {
         const int s = u0 / p.T, ta = u0 - s * p.T, tb = min(p.T, ta + (u1 - u0));
 #pragma unroll
-        for (int d = 0; d < kRing; ++d) {
+        for (int d = 0; d < RING; ++d) {
             const int t = ta + warp + kDecodeWarps * d;
             if (u0 < u1 && t < tb) load_tile(p, s, t, lane, rb[d], rs[d]);
         }
@@ -496,23 +540,38 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
         const int tb = min(p.T, ta + (u1 - u));
         u += tb - ta;
 
-        for (int m = 0; m < p.M; ++m) {
-            __syncthreads();  // the previous table is no longer read
+        // Tokens two at a time: both tables are built, then every weight tile
+        // loaded serves both tokens' lookups.
+        for (int m = 0; m < p.M; m += TWO ? 2 : 1) {
+            const bool two = TWO && m + 1 < p.M;
+            __syncthreads();  // the previous tables are no longer read
             if (!preloaded) {
                 slice_load_signs(p, s, warp, lane, xv);
 #pragma unroll
-                for (int d = 0; d < kRing; ++d) {
+                for (int d = 0; d < RING; ++d) {
                     const int t = ta + warp + kDecodeWarps * d;
                     if (t < tb) load_tile(p, s, t, lane, rb[d], rs[d]);
                 }
             }
             preloaded = false;
+            float xv2[4 * kRowsPerWarp];
+#pragma unroll
+            for (int i = 0; i < 4 * kRowsPerWarp; ++i) xv2[i] = xv[i];  // the signs
             slice_load_x(p, m, s, warp, lane, xv);
+            if (two) slice_load_x(p, m + 1, s, warp, lane, xv2);
             slice_transform_rows(s, xv, tbuf, warp, lane);
             __syncthreads();
             slice_transform_cols(tbuf, xs, warp, lane);
             __syncthreads();
             build_tables(xs, lut, warp, lane);
+            if (two) {
+                __syncthreads();  // tbuf and xs are free again
+                slice_transform_rows(s, xv2, tbuf, warp, lane);
+                __syncthreads();
+                slice_transform_cols(tbuf, xs, warp, lane);
+                __syncthreads();
+                build_tables(xs, lut2, warp, lane);
+            }
             __syncthreads();
             // The next kernel may launch now: its weight prefetch then overlaps
             // this kernel's lookups rather than its latency-bound prologue.
@@ -520,27 +579,38 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
                 pdl_launch_dependents();
                 triggered = true;
             }
-            // Partial sums: tile t, lane -> part[(t - tbase) * 32 + lane].
+            // Partial sums: tile t, lane -> part[(t - tbase) * 32 + lane]; the
+            // second token's are `pstep` floats further.
             float* part = p.cluster ? pbuf + (size_t)m * (tb - ta) * kTileRows
                                     : p.partials + ((size_t)s * p.M + m) * npad;
+            const size_t pstep = p.cluster ? (size_t)(tb - ta) * kTileRows : npad;
             const int tbase = p.cluster ? ta : 0;
-            for (int j0 = 0;; j0 += kRing) {
+            for (int j0 = 0;; j0 += RING) {
                 bool more = true;
 #pragma unroll
-                for (int d = 0; d < kRing; d += 2) {
+                for (int d = 0; d < RING; d += 2) {
                     const int t0 = ta + warp + kDecodeWarps * (j0 + d);
                     const int t1 = t0 + kDecodeWarps;
                     if (t0 >= tb) {
                         more = false;
                         break;
                     }
-                    float v0, v1;
-                    tile_dot2(lut, rb[d], rs[d], rb[d + 1], rs[d + 1], base_off, v0, v1);
-                    const int tn0 = t0 + kDecodeWarps * kRing, tn1 = t1 + kDecodeWarps * kRing;
+                    float v0, v1, w0 = 0.f, w1 = 0.f;
+                    if (two) {
+                        tile_dot_two(lut, lut2, rb[d], rs[d], base_off, v0, w0);
+                        tile_dot_two(lut, lut2, rb[d + 1], rs[d + 1], base_off, v1, w1);
+                    } else {
+                        tile_dot2(lut, rb[d], rs[d], rb[d + 1], rs[d + 1], base_off, v0, v1);
+                    }
+                    const int tn0 = t0 + kDecodeWarps * RING, tn1 = t1 + kDecodeWarps * RING;
                     if (tn0 < tb) load_tile(p, s, tn0, lane, rb[d], rs[d]);
                     if (tn1 < tb) load_tile(p, s, tn1, lane, rb[d + 1], rs[d + 1]);
                     part[(size_t)(t0 - tbase) * kTileRows + lane] = v0;
                     if (t1 < tb) part[(size_t)(t1 - tbase) * kTileRows + lane] = v1;
+                    if (two) {
+                        part[pstep + (size_t)(t0 - tbase) * kTileRows + lane] = w0;
+                        if (t1 < tb) part[pstep + (size_t)(t1 - tbase) * kTileRows + lane] = w1;
+                    }
                 }
                 if (!more) break;
             }
@@ -583,8 +653,8 @@ int max_clusters(int S, int num_sms)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0, per_sm = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, bitlin_decode_gemv, &cfg) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bitlin_decode_gemv, kDecodeThreads,
+    if (cudaOccupancyMaxActiveClusters(&n, bitlin_decode_gemv<false>, &cfg) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bitlin_decode_gemv<false>, kDecodeThreads,
                                                       kPbufOff + kPbufBytes) != cudaSuccess) {
         (void)cudaGetLastError();
         n = 0;
@@ -604,16 +674,17 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess && g_max_smem < kDecodeSmem) e = cudaErrorInvalidConfiguration;
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(bitlin_decode_gemv, cudaFuncAttributeMaxDynamicSharedMemorySize, g_max_smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(bitlin_decode_gemv, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e == cudaSuccess && g_max_smem < kPbufOff2) e = cudaErrorInvalidConfiguration;
+        for (auto k : {bitlin_decode_gemv<false>, bitlin_decode_gemv<true>}) {
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g_max_smem);
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        }
         if (e != cudaSuccess) return e;
         configured = true;
     }
     DecodeParams q = p;
-    int grid, smem = kDecodeSmem, cluster = 0;
+    const int base_smem = p.M >= 2 ? kPbufOff2 : kDecodeSmem;  // two tables from M = 2
+    int grid, smem = base_smem, cluster = 0;
     q.cluster = 0;
     // Split-K across a cluster when the slices fit one (S <= 16) and the
     // partial sums fit shared memory; else through the global scratch.
@@ -622,11 +693,12 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
         if (maxc > 0) {
             const int ncl = maxc < p.T ? maxc : p.T;
             const long long pb = (long long)p.M * ((p.T + ncl - 1) / ncl) * kTileRows * 4;
-            if (pb <= kPbufBytes && kPbufOff + pb <= g_max_smem) {
+            const int poff = p.M >= 2 ? kPbufOff2 : kPbufOff;
+            if (pb <= kPbufBytes && poff + pb <= g_max_smem) {
                 q.cluster = 1;
                 q.ctas_per_slice = ncl;
                 grid = p.S * ncl;
-                smem = kPbufOff + (int)pb;
+                smem = poff + (int)pb;
                 cluster = p.S;
             }
         }
@@ -657,5 +729,6 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = cluster ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, bitlin_decode_gemv, q);
+    return p.M >= 2 ? cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<true>, q)
+                    : cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<false>, q);
 }
