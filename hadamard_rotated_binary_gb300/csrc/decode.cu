@@ -1,5 +1,6 @@
-// Decode GEMV (M < 64): activation rotation fused into the prologue, then the
-// one-bit product through shared-memory signed-sum tables.
+// Decode GEMV (the library's choice for M <= 4; any M when forced): activation
+// rotation fused into the prologue, then the one-bit product through
+// shared-memory signed-sum tables.
 //
 // Method (what is computed) - Pulse "ARCHITECTURE-SPEC", Hadamard-fold
 // section: xt = WHT1024(signs * P(x)) / 32 per 1024-block, then y = W @ xt;
@@ -9,11 +10,17 @@
 // How (GB300 design):
 //  * Work unit = (slice s of 512 weights along K) x (tile t of 32 rows).  A CTA
 //    (16 warps, one per SM) owns one slice and a contiguous range of tiles.
-//    Split-K partial sums land in a scratch array; at the end each CTA takes
-//    one ticket per tile in parallel, and the CTA that draws the last ticket
-//    of a tile sums its S partials in fixed order s = 0..S-1 (deterministic)
-//    with all of its threads.  One kernel per call, so that programmatic
-//    dependent launch can overlap consecutive calls.
+//    Split-K: when the S slices of a tile range fit a thread-block cluster
+//    (S <= 16) and their partial sums fit shared memory, the S CTAs form a
+//    cluster, keep their partials in shared memory and sum them through
+//    distributed shared memory (cluster_finish).  Otherwise the partials land
+//    in a scratch array, each CTA takes one ticket per tile in parallel, and
+//    the CTA that draws the last ticket of a tile sums the tile (splitk_finish).
+//    Both sum in the fixed order s = 0..S-1 (deterministic).  One kernel per
+//    call, so that programmatic dependent launch can overlap consecutive calls.
+//  * Tokens: one at a time for M = 1; two at a time otherwise (a separate
+//    instance with both tables built and a 2-deep register ring, so that every
+//    weight tile loaded serves two tokens).
 //  * Prologue per (token, slice): gather x (with the ssm_out permutation when
 //    requested), multiply by the signs, and form the 512 outputs of the
 //    1024-point transform that the slice needs: with H1024 = [[H, H], [H, -H]],
@@ -337,8 +344,7 @@ constexpr int kPrefetchUnits = 64;
 #endif
 constexpr int kRing = BITLIN_DECODE_RING;
 
-// Registers per thread: with 8 warps per CTA two CTAs (this call's and the
-// next call's) fit in an SM's 65,536 registers.
+// Registers per thread: 16 warps x 128 = the SM's 65,536 (one CTA per SM).
 #ifndef BITLIN_DECODE_REGS
 #define BITLIN_DECODE_REGS 128
 #endif
