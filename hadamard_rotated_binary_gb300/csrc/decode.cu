@@ -287,6 +287,31 @@ __device__ __forceinline__ void tile_dot2(const unsigned char* lut, const uint4 
     out1 = acc1;
 }
 
+// One tile (a warp's last, odd one): four independent lookup chains, half the
+// work of tile_dot2, the same arithmetic per tile.
+__device__ __forceinline__ void tile_dot1(const unsigned char* lut, const uint4 (&b)[4], uint2 sc,
+                                          uint32_t base_off, float& out)
+{
+    float acc = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const uint32_t w[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+        float g0 = 0.f, g1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t pos = 4u * u + c;
+            const uint32_t off = base_off ^ ((4u * pos) * 0x101u);
+            g0 += lut_at(lut, __byte_perm(w[c], off, 0x7604));
+            g1 += lut_at(lut, __byte_perm(w[c], off, 0x7615));
+            g0 += lut_at(lut + 128, __byte_perm(w[c], off, 0x7624));
+            g1 += lut_at(lut + 128, __byte_perm(w[c], off, 0x7635));
+        }
+        const float sv = __half2float(__ushort_as_half((unsigned short)((u < 2 ? sc.x : sc.y) >> (16 * (u & 1)))));
+        acc = fmaf(g0 + g1, sv, acc);
+    }
+    out = acc;
+}
+
 // One tile against two tokens' tables: every byte's shared-memory offset is
 // built once and read in both tables (the second at lut2), so each loaded
 // weight tile serves two tokens.
@@ -601,12 +626,14 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
                         more = false;
                         break;
                     }
-                    float v0, v1, w0 = 0.f, w1 = 0.f;
+                    float v0, v1 = 0.f, w0 = 0.f, w1 = 0.f;
                     if (two) {
                         tile_dot_two(lut, lut2, rb[d], rs[d], base_off, v0, w0);
-                        tile_dot_two(lut, lut2, rb[d + 1], rs[d + 1], base_off, v1, w1);
-                    } else {
+                        if (t1 < tb) tile_dot_two(lut, lut2, rb[d + 1], rs[d + 1], base_off, v1, w1);
+                    } else if (t1 < tb) {
                         tile_dot2(lut, rb[d], rs[d], rb[d + 1], rs[d + 1], base_off, v0, v1);
+                    } else {
+                        tile_dot1(lut, rb[d], rs[d], base_off, v0);
                     }
                     const int tn0 = t0 + kDecodeWarps * RING, tn1 = t1 + kDecodeWarps * RING;
                     if (tn0 < tb) load_tile(p, s, tn0, lane, rb[d], rs[d]);
