@@ -460,34 +460,32 @@ __device__ __forceinline__ void splitk_finish(const DecodeParams& p, int ta, int
     }
 }
 
-// Split-K across a cluster: CTA rank s of the cluster holds slice s's partial
-// sums of the cluster's tiles [ta, tb) in its own shared memory (pbuf,
-// [M][tb - ta][32]).  After a cluster barrier each CTA sums an equal share of
-// the rows over all S CTAs, in slice order s = 0..S-1 (the same order and
-// arithmetic as the global-scratch path), and writes y.  A second barrier
-// keeps every CTA's shared memory alive until the others have read it.
+// Split-K across a cluster.  The cluster's tiles [ta, tb) are dealt round
+// robin to its S CTAs: local tile lt belongs to CTA lt % S, slot lt / S.  Every
+// CTA stores each partial sum of its slice straight into the owner's shared
+// memory as it computes it (pbuf [M][S][LT][32], LT = ceil((tb - ta) / S)).
+// After one cluster barrier, which makes those stores visible, each CTA sums
+// its own tiles over the S slices in slice order s = 0..S-1 (the same order
+// and arithmetic as the global-scratch path) from its own shared memory, and
+// writes y.  Nothing reads another CTA's shared memory after the barrier, so
+// no second barrier is needed before the CTAs exit.
+__device__ __forceinline__ int cluster_slots(int ntile, int S) { return (ntile + S - 1) / S; }
+
 __device__ __forceinline__ void cluster_finish(const DecodeParams& p, int ta, int tb, int rank, const float* pbuf)
 {
     ptx::cluster_sync();
-    const int ntile = tb - ta;
-    const int rows = p.M * ntile * kTileRows;
-    const int lo = (int)((long long)rows * rank / p.S), hi = (int)((long long)rows * (rank + 1) / p.S);
-    const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(pbuf));
-    for (int i = lo + (int)threadIdx.x; i < hi; i += kDecodeThreads) {
-        const uint32_t a = base + 4u * (uint32_t)i;
-        float v[kMaxClusterSlices];
-#pragma unroll
-        for (int j = 0; j < kMaxClusterSlices; ++j)
-            if (j < p.S) v[j] = ptx::ld_cluster(ptx::cluster_map(a, j));
+    const int ntile = tb - ta, S = p.S, LT = cluster_slots(ntile, S);
+    const int mine = ntile > rank ? (ntile - rank + S - 1) / S : 0;  // tiles rank, rank + S, ...
+    const int rows = p.M * mine * kTileRows;
+    for (int i = (int)threadIdx.x; i < rows; i += kDecodeThreads) {
+        const int m = i / (mine * kTileRows), rem = i - m * mine * kTileRows;
+        const int slot = rem / kTileRows, lane = rem - slot * kTileRows;
+        const float* src = pbuf + (((size_t)m * S) * LT + slot) * kTileRows + lane;
         float sum = 0.f;
-#pragma unroll
-        for (int j = 0; j < kMaxClusterSlices; ++j)
-            if (j < p.S) sum += v[j];
-        const int m = i / (ntile * kTileRows), r = i - m * ntile * kTileRows;
-        const int n = ta * kTileRows + r;
+        for (int s = 0; s < S; ++s) sum += src[(size_t)s * LT * kTileRows];
+        const int n = (ta + slot * S + rank) * kTileRows + lane;
         if (n < p.N) p.y[(size_t)m * p.N + n] = sum;
     }
-    ptx::cluster_sync();
 }
 
 // TWO: tokens are taken two at a time (M >= 2), with a 2-deep register ring so
@@ -610,12 +608,20 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
                 pdl_launch_dependents();
                 triggered = true;
             }
-            // Partial sums: tile t, lane -> part[(t - tbase) * 32 + lane]; the
-            // second token's are `pstep` floats further.
-            float* part = p.cluster ? pbuf + (size_t)m * (tb - ta) * kTileRows
-                                    : p.partials + ((size_t)s * p.M + m) * npad;
-            const size_t pstep = p.cluster ? (size_t)(tb - ta) * kTileRows : npad;
-            const int tbase = p.cluster ? ta : 0;
+            // Partial sums.  Scratch path: token mm, tile t, lane ->
+            // partials[s][mm][t * 32 + lane].  Cluster path: into the owner's shared
+            // memory (see cluster_finish).
+            const int LT = cluster_slots(tb - ta, p.S);
+            const uint32_t pbase = static_cast<uint32_t>(__cvta_generic_to_shared(pbuf));
+            auto put = [&](int mm, int t, float v) {
+                if (p.cluster) {
+                    const int lt = t - ta;
+                    const uint32_t off = (uint32_t)((((mm * p.S) + rank) * LT + lt / p.S) * kTileRows + lane);
+                    ptx::st_cluster(ptx::cluster_map(pbase + 4u * off, lt % p.S), v);
+                } else {
+                    p.partials[((size_t)s * p.M + mm) * npad + (size_t)t * kTileRows + lane] = v;
+                }
+            };
             for (int j0 = 0;; j0 += RING) {
                 bool more = true;
 #pragma unroll
@@ -638,11 +644,11 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
                     const int tn0 = t0 + kDecodeWarps * RING, tn1 = t1 + kDecodeWarps * RING;
                     if (tn0 < tb) load_tile(p, s, tn0, lane, rb[d], rs[d]);
                     if (tn1 < tb) load_tile(p, s, tn1, lane, rb[d + 1], rs[d + 1]);
-                    part[(size_t)(t0 - tbase) * kTileRows + lane] = v0;
-                    if (t1 < tb) part[(size_t)(t1 - tbase) * kTileRows + lane] = v1;
+                    put(m, t0, v0);
+                    if (t1 < tb) put(m, t1, v1);
                     if (two) {
-                        part[pstep + (size_t)(t0 - tbase) * kTileRows + lane] = w0;
-                        if (t1 < tb) part[pstep + (size_t)(t1 - tbase) * kTileRows + lane] = w1;
+                        put(m + 1, t0, w0);
+                        if (t1 < tb) put(m + 1, t1, w1);
                     }
                 }
                 if (!more) break;
@@ -725,7 +731,8 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
         const int maxc = max_clusters(p.S, num_sms);
         if (maxc > 0) {
             const int ncl = maxc < p.T ? maxc : p.T;
-            const long long pb = (long long)p.M * ((p.T + ncl - 1) / ncl) * kTileRows * 4;
+            const int lt = ((p.T + ncl - 1) / ncl + p.S - 1) / p.S;  // slots per CTA
+            const long long pb = (long long)p.M * p.S * lt * kTileRows * 4;
             const int poff = p.M >= 2 ? kPbufOff2 : kPbufOff;
             if (pb <= kPbufBytes && poff + pb <= g_max_smem) {
                 q.cluster = 1;

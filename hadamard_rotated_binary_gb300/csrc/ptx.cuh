@@ -163,6 +163,11 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, int rank)
     return r;
 }
 
+__device__ __forceinline__ void st_cluster(uint32_t caddr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ float ld_cluster(uint32_t caddr)
 {
     float v;
