@@ -170,13 +170,18 @@ def path_of(w: synth.Workload, path: str = "auto") -> str:
     return "bitlin_decode_gemv" if uses_decode(w, path) else "bitlin_tc_gemm"
 
 
-def roofline(w: synth.Workload, s_per_step: float, peaks: dict, peak_kind: str, path: str = "auto") -> dict:
-    """Roofline of the dominant kernel.  M = 1: HBM-bound, algorithmic bytes per launch over the
-    launch time (one launch per step).  M >= 2: the tensor-core GEMM, 2*M*N*K bf16 MMA flops per
-    launch (the exact path multiplies three bf16 digit columns per token, 3x that) over the step
-    time, which also holds the small rotation kernel, so the fraction is a lower bound; peak = the
-    measured burst bf16 GEMM rate (the timed loop lasts milliseconds)."""
+def roofline(w: synth.Workload, s_per_step: float, peaks: dict, peak_kind: str, path: str = "auto",
+             kernels: int = 1) -> dict:
+    """Roofline of the dominant kernel.  Decode: HBM-bound, algorithmic bytes per call over the
+    step time (one GEMV per step; with kernels = 2 the step also holds the small split-K sum,
+    which the GEMV overlaps through programmatic dependent launch, so the fraction is a lower
+    bound).  Tensor paths: the tcgen05 GEMM, 2*M*N*K bf16 MMA flops per launch (the exact path
+    multiplies three bf16 digit columns per token, 3x that) over the step time, which also holds
+    the small rotation kernel, so the fraction is a lower bound; peak = the measured burst bf16
+    GEMM rate (the timed loop lasts milliseconds)."""
     kernel = path_of(w, path)
+    if uses_decode(w, path) and kernels == 2:
+        kernel = "bitlin_decode_gemv + bitlin_decode_reduce"
     if uses_decode(w, path):
         achieved = w.algorithmic_bytes() / s_per_step / 1e9
         return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -352,9 +357,12 @@ def run_op(args, ws, rank, local, pg):
         s_step = ms / 1e3 / args.steps
         algo = wbytes + 4 * M * wgu.K + 4 * M * wdn.N + 4 * (wgu.K + wdn.K)
         flops = 2.0 * M * (wgu.N * wgu.K + wdn.N * wdn.K)
-        if M == 1:
+        (pgu, kgu), (pdn, kdn) = pairs[0][0].plan(M), pairs[0][1].plan(M)
+        kernels = kgu + kdn
+        if pgu == pdn == hrb.PATH_DECODE:
             roof = {"bound": "hbm", "achieved": algo / s_step / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "kernel": "bitlin_decode_gemv (x2)", "bytes_per_launch": algo}
+                    "kernel": "bitlin_decode_gemv (x2)" + " + bitlin_decode_reduce" * (kernels - 2),
+                    "bytes_per_launch": algo}
         else:
             digits = 3 if M < 64 else 1
             roof = {"bound": "tensor", "achieved": digits * flops / s_step / 1e12, "peak": peaks["bf16_tflops"],
@@ -363,7 +371,7 @@ def run_op(args, ws, rank, local, pg):
         metric, config = MLP_METRIC, {"workload": "mlp_block", "M": M, "hidden": wgu.K, "ffn": wdn.K,
                                       "weight_copies": R, "weight_set_bytes": R * wbytes,
                                       "l2": f"inputs larger than L2: {R} distinct weight pairs cycled"}
-        launches = 2 if M == 1 else 4
+        launches = kernels
         wgb = wbytes / s_step / 1e9
 
         def e2e_call(xh, yh):
@@ -403,9 +411,11 @@ def run_op(args, ws, rank, local, pg):
         ms, clocks = timed_graph(step, stream, args.steps, max(args.warmup, R), pg, dev)
         s_step = ms / 1e3 / args.steps
         algo = wbytes + 4 * M * K + 4 * M * N + 4 * K + 4 * M
-        if M == 1:
+        hpath, hk = heads[0].plan(M)
+        if hpath == hrb.PATH_DECODE:
             roof = {"bound": "hbm", "achieved": algo / s_step / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "kernel": "bitlin_decode_gemv + bitlin_argmax_rows", "bytes_per_launch": algo}
+                    "kernel": "bitlin_decode_gemv" + " + bitlin_decode_reduce" * (hk - 1) + " + bitlin_argmax_rows",
+                    "bytes_per_launch": algo}
         else:
             digits = 3 if M < 64 else 1
             flops = 2.0 * M * digits * N * K
@@ -415,7 +425,7 @@ def run_op(args, ws, rank, local, pg):
         metric, config = LMHEAD_METRIC, {"workload": "lm_head", "M": M, "N": N, "K": K, "weight_copies": R,
                                          "weight_set_bytes": R * wbytes,
                                          "l2": f"inputs larger than L2: {R} distinct copies cycled"}
-        launches, wgb = (2 if M == 1 else 3), wbytes / s_step / 1e9
+        launches, wgb = hk + 1, wbytes / s_step / 1e9
 
         def e2e_call(xh, yh):
             xd.copy_(xh, non_blocking=True)
@@ -627,6 +637,7 @@ def main():
 
     peaks, peak_kind = measured_peaks()
     s_per_step = ms / 1e3 / args.steps
+    kernels = layers[0].plan(w.M)[1]
     tokens_per_s = ws * w.M / s_per_step
     algo_bytes = w.algorithmic_bytes()
     achieved = algo_bytes / s_per_step / 1e9
@@ -649,8 +660,8 @@ def main():
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "weight_gbs": w.weight_bytes() / s_per_step / 1e9,
         "hbm_frac_of_8tbs": achieved / 8000.0,
-        "roofline": roofline(w, s_per_step, peaks, peak_kind, args.path),
-        "gpu_launches": args.steps * (1 if uses_decode(w, args.path) else 2),  # GEMV; or rotate + GEMM
+        "roofline": roofline(w, s_per_step, peaks, peak_kind, args.path, kernels),
+        "gpu_launches": args.steps * kernels,  # the library's own count per call (bitlin_plan)
         "clocks": clocks,
         "e2e": {"value": ws * w.M * e2e_steps / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": 4 * w.M * w.K, "d2h_bytes_per_step": 4 * w.M * w.N,

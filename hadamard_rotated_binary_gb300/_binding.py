@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
     L.bitlin_mlp_forward.argtypes = [P, P, P, i32, P, P]
     L.bitlin_argmax.argtypes = [P, P, i32, P, P, P]
     L.bitlin_set_path.argtypes = [P, i32]
+    L.bitlin_plan.argtypes = [P, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
     L.bitlin_set_wait_budget.argtypes = [P, i64]
     L.bitlin_test_stall.argtypes = [P, i32]
     L.bitlin_destroy.argtypes = [P]
@@ -76,8 +77,8 @@ def lib() -> ctypes.CDLL:
     L.bitlin_cuda_error.argtypes = [P]
     L.bitlin_status_string.argtypes = [i32]
     L.bitlin_status_string.restype = ctypes.c_char_p
-    for name in ("bitlin_create", "bitlin_forward", "bitlin_forward_host", "bitlin_embed", "bitlin_mlp_forward", "bitlin_argmax", "bitlin_set_path",
-                 "bitlin_set_wait_budget", "bitlin_test_stall", "bitlin_destroy", "bitlin_get_error",
+    for name in ("bitlin_create", "bitlin_forward", "bitlin_forward_host", "bitlin_embed", "bitlin_mlp_forward",
+                 "bitlin_argmax", "bitlin_set_path", "bitlin_plan", "bitlin_set_wait_budget", "bitlin_test_stall", "bitlin_destroy", "bitlin_get_error",
                  "bitlin_cuda_error", "bitlin_version"):
         getattr(L, name).restype = i32
     _lib = L
@@ -209,6 +210,12 @@ class BitLinear:
 
     def set_path(self, path: int):
         self._check(lib().bitlin_set_path(self._h, int(path)), "bitlin_set_path")
+
+    def plan(self, M: int) -> tuple[int, int]:
+        """bitlin_plan: (path, kernels launched) of a forward call with M tokens."""
+        path, kernels = ctypes.c_int32(), ctypes.c_int32()
+        self._check(lib().bitlin_plan(self._h, int(M), ctypes.byref(path), ctypes.byref(kernels)), "bitlin_plan")
+        return path.value, kernels.value
 
     def set_wait_budget(self, ns: int):
         self._check(lib().bitlin_set_wait_budget(self._h, int(ns)), "bitlin_set_wait_budget")

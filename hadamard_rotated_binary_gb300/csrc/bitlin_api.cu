@@ -41,7 +41,6 @@ void release(bitlin_t h)
     free_dev(h->pscales);
     free_dev(h->signs);
     free_dev(h->partials);
-    free_dev(h->counters);
     free_dev(h->xt);
     free_dev(h->dev_error);
     free_dev(h->hx);
@@ -112,10 +111,8 @@ bitlin_status ensure_xt(bitlin_t h, int M, int exact)
     return BITLIN_OK;
 }
 
-bitlin_status run_decode(bitlin_t h, const float* x, int M, float* y, cudaStream_t s, int swiglu = 0)
+DecodeParams decode_params(bitlin_t h, const float* x, int M, float* y, int swiglu)
 {
-    cudaError_t e = ensure_partials(h, M);
-    if (e != cudaSuccess) return from_cuda(h, e);
     DecodeParams p;
     p.bits = h->dbits;
     p.scales = h->dscales;
@@ -123,7 +120,6 @@ bitlin_status run_decode(bitlin_t h, const float* x, int M, float* y, cudaStream
     p.x = x;
     p.y = y;
     p.partials = h->partials;
-    p.counters = h->counters;
     p.M = M;
     p.N = h->N;
     p.K = h->K;
@@ -134,7 +130,14 @@ bitlin_status run_decode(bitlin_t h, const float* x, int M, float* y, cudaStream
     p.cluster = 0;
     p.allow_cluster = 1;
     p.swiglu = swiglu;
-    return from_cuda(h, bitlin_launch_decode(p, h->num_sms, s));
+    return p;
+}
+
+bitlin_status run_decode(bitlin_t h, const float* x, int M, float* y, cudaStream_t s, int swiglu = 0)
+{
+    cudaError_t e = ensure_partials(h, M);
+    if (e != cudaSuccess) return from_cuda(h, e);
+    return from_cuda(h, bitlin_launch_decode(decode_params(h, x, M, y, swiglu), h->num_sms, s));
 }
 
 bitlin_status run_tc(bitlin_t h, const float* x, int M, float* y, cudaStream_t s, int exact, int swiglu = 0)
@@ -231,12 +234,10 @@ bitlin_status bitlin_create(bitlin_t* out, int N, int K, const uint32_t* packed_
     BITLIN_TRY(cudaMalloc(&h->pbits, words * sizeof(uint32_t)));
     BITLIN_TRY(cudaMalloc(&h->pscales, groups * sizeof(uint16_t)));
     BITLIN_TRY(cudaMalloc(&h->signs, (size_t)K * sizeof(float)));
-    BITLIN_TRY(cudaMalloc(&h->counters, (size_t)h->T * kTicketStride * sizeof(unsigned)));
     BITLIN_TRY(cudaMalloc(&h->dev_error, 2 * sizeof(int)));
     BITLIN_TRY(cudaHostAlloc(&h->h_err, sizeof(int), cudaHostAllocDefault));
     bad = h->dev_error + 1;
     BITLIN_TRY(cudaMemsetAsync(h->dev_error, 0, 2 * sizeof(int), st));
-    BITLIN_TRY(cudaMemsetAsync(h->counters, 0, (size_t)h->T * kTicketStride * sizeof(unsigned), st));
     BITLIN_TRY(cudaMemcpyAsync(h->signs, signs, (size_t)K * sizeof(float), cudaMemcpyDeviceToDevice, st));
     BITLIN_TRY(cudaMemcpyAsync(h->pscales, scales, groups * sizeof(uint16_t), cudaMemcpyDeviceToDevice, st));
     BITLIN_TRY(bitlin_launch_check_signs(h->signs, K, bad, st));
@@ -325,6 +326,17 @@ bitlin_status run_path(bitlin_t h, const float* x, int M, float* y, cudaStream_t
 }
 
 }  // namespace
+
+bitlin_status bitlin_plan(bitlin_t h, int M, int* path, int* kernels)
+{
+    if (!h || !path || !kernels || M < 1) return BITLIN_EINVAL;
+    *path = choose_path(h, M);
+    if (*path != BITLIN_PATH_DECODE) {
+        *kernels = 2;  // the rotation into bf16, then the tensor-core GEMM
+        return BITLIN_OK;
+    }
+    return from_cuda(h, bitlin_decode_kernels(decode_params(h, nullptr, M, nullptr, 0), h->num_sms, kernels));
+}
 
 bitlin_status bitlin_forward(bitlin_t h, const float* x, int M, float* y, bitlin_stream_t stream)
 {

@@ -21,7 +21,6 @@ constexpr int kGroupsPerSlice = 4;    // 128-weight scale groups per slice
 constexpr int kDecodeThreads = BITLIN_DECODE_THREADS;  // 16 warps per CTA, one CTA per SM
 constexpr int kDecodeWarps = kDecodeThreads / 32;
 constexpr int kLutBytes = 65536;      // 64 octet tables x 256 entries x f32
-constexpr int kTicketStride = 32;     // one split-K ticket per 128-byte line
 
 // ---- prefill layout ------------------------------------------------------
 constexpr int kPrefillRows = 128;     // weight rows per CTA (UMMA M)
@@ -42,8 +41,7 @@ struct DecodeParams {
     const float* signs;     // [K]
     const float* x;         // [M][K]
     float* y;               // [M][N]
-    float* partials;        // [S][M][T*32], fully rewritten by every call
-    unsigned* counters;     // [T * kTicketStride] split-K tickets, zero between calls
+    float* partials;        // [S][M][T*32], fully rewritten by every call (scratch split-K)
     int M, N, K, S, T, perm;
     int ctas_per_slice;     // set by the launcher
     int cluster;            // set by the launcher: 1 = split-K summed across a thread-block cluster
@@ -83,7 +81,6 @@ struct bitlin {
     // scratch
     float* partials = nullptr;
     int partials_M = 0;
-    unsigned* counters = nullptr;
     void* xt = nullptr;        // bf16 [M][K] rotated activations for the prefill path
     int xt_M = 0;
     alignas(64) unsigned char tmap[128];       // TMA descriptor of xt (a CUtensorMap)
@@ -119,6 +116,8 @@ cudaError_t bitlin_launch_repack_prefill(const uint32_t* bits, int N, int K, uin
                                          cudaStream_t s);
 cudaError_t bitlin_launch_check_signs(const float* signs, int K, int* bad, cudaStream_t s);
 cudaError_t bitlin_launch_decode(const bitlin_impl::DecodeParams& p, int num_sms, cudaStream_t s);
+// Kernels one bitlin_launch_decode of p launches: 1 (cluster split-K) or 2 (GEMV, then the sum).
+cudaError_t bitlin_decode_kernels(const bitlin_impl::DecodeParams& p, int num_sms, int* kernels);
 cudaError_t bitlin_launch_argmax(const float* y, int M, int N, void* cand, unsigned* tickets, int32_t* ids,
                                  cudaStream_t s);
 size_t bitlin_argmax_scratch_bytes(int M);

@@ -14,10 +14,9 @@
 //    (S <= 16) and their partial sums fit shared memory, the S CTAs form a
 //    cluster, keep their partials in shared memory and sum them through
 //    distributed shared memory (cluster_finish).  Otherwise the partials land
-//    in a scratch array, each CTA takes one ticket per tile in parallel, and
-//    the CTA that draws the last ticket of a tile sums the tile (splitk_finish).
-//    Both sum in the fixed order s = 0..S-1 (deterministic).  One kernel per
-//    call, so that programmatic dependent launch can overlap consecutive calls.
+//    in a scratch array and a second kernel (bitlin_decode_reduce, chained by
+//    programmatic dependent launch) sums every output over the slices with
+//    one thread each.  Both sum in the fixed order s = 0..S-1 (deterministic).
 //  * Tokens: one at a time for M = 1; two at a time otherwise (a separate
 //    instance with both tables built and a 2-deep register ring, so that every
 //    weight tile loaded serves two tokens).
@@ -63,8 +62,7 @@ using namespace bitlin_impl;
 constexpr int kPad = 33;                               // transpose row stride (floats)
 constexpr int kSmemTranspose = 16 * kPad * 4;           // 2112 B
 constexpr int kSmemSlice = (kSlice + kSlice / 32) * 4;  // 528 floats
-constexpr int kMaxList = 1024;                          // finished-tile list (ints)
-constexpr int kDecodeSmem = kLutBytes + kSmemTranspose + kSmemSlice + (kMaxList + 1) * 4;
+constexpr int kDecodeSmem = kLutBytes + kSmemTranspose + kSmemSlice;
 // With M >= 2 a second 64 KB table follows (tokens are taken two at a time),
 // then, for the cluster split-K, the CTA's partial sums [M][tiles][32].
 constexpr int kLut2Off = (kDecodeSmem + 127) & ~127;
@@ -375,91 +373,6 @@ constexpr int kRing = BITLIN_DECODE_RING;
 #endif
 constexpr int kDecodeRegs = BITLIN_DECODE_REGS;
 
-// End of a segment [ta, tb) of one slice: publish the partial sums, take one
-// ticket per tile (in parallel, one thread each), and reduce the tiles whose
-// S-th ticket this CTA drew: every output row of those tiles is the sum of its
-// S partials in slice order s = 0..S-1 (deterministic).
-// Ordering: the tickets are acquire-release atomics taken after a CTA barrier
-// and followed by one, so the partial stores of every slice happen before the
-// loads of whichever CTA completes a tile.  The finished tiles' partials are staged into shared memory
-// (the table area, free by then) with asynchronous 16-byte copies, all in
-// flight at once, then summed in slice order.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-                 "l"(src)
-                 : "memory");
-}
-
-// One split-K ticket: atomic increment at GPU scope with release semantics
-// (the CTA's partial stores, ordered before it by the preceding barrier, are
-// visible to whoever observes the increment) and acquire semantics (the
-// partials of the other slices, released by their tickets, are visible to
-// this CTA's loads after the following barrier).
-__device__ __forceinline__ unsigned ticket_acq_rel(unsigned* addr)
-{
-    unsigned old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(addr) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ void splitk_finish(const DecodeParams& p, int ta, int tb, size_t npad,
-                                              int* done_list, int* done_count, float* stage)
-{
-    __syncthreads();  // every partial store is done, and every warp is done reading the tables
-    const int ntiles = tb - ta;
-    const int per_batch = kLutBytes / (p.S * kTileRows * 4);  // tiles whose S partials fit
-    for (int base = 0; base < ntiles; base += kMaxList) {
-        const int chunk = min(kMaxList, ntiles - base);
-        if (threadIdx.x == 0) *done_count = 0;
-        __syncthreads();
-        for (int i = threadIdx.x; i < chunk; i += kDecodeThreads) {
-            const int t = ta + base + i;
-            if (ticket_acq_rel(p.counters + (size_t)t * kTicketStride) == (unsigned)(p.S - 1)) {
-                p.counters[(size_t)t * kTicketStride] = 0u;  // rearm for the next call
-                done_list[atomicAdd(done_count, 1)] = t;
-            }
-        }
-        __syncthreads();
-        const int ndone = *done_count;
-        for (int m = 0; m < p.M; ++m) {
-            for (int b0 = 0; b0 < ndone; b0 += per_batch) {
-                const int nb = min(per_batch, ndone - b0);
-                const int pieces = p.S * nb * (kTileRows / 4);  // 16-byte pieces
-                for (int c = threadIdx.x; c < pieces; c += kDecodeThreads) {
-                    const int sl = c / (nb * 8), rem = c - sl * nb * 8;
-                    const int ti = rem >> 3, q = rem & 7;
-                    const float* src = p.partials + ((size_t)sl * p.M + m) * npad +
-                                       (size_t)done_list[b0 + ti] * kTileRows + 4 * q;
-                    cp_async16(stage + ((size_t)sl * nb + ti) * kTileRows + 4 * q, src);
-                }
-                asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-                __syncthreads();
-                for (int r = threadIdx.x; r < nb * kTileRows; r += kDecodeThreads) {
-                    const int ti = r >> 5, lane = r & 31;
-                    const float* col = stage + (size_t)ti * kTileRows + lane;
-                    const int sstep = nb * kTileRows;
-                    float sum = 0.f;
-                    int sl = 0;
-                    for (; sl + 4 <= p.S; sl += 4) {
-                        const float a = col[(size_t)sl * sstep], b = col[(size_t)(sl + 1) * sstep];
-                        const float c = col[(size_t)(sl + 2) * sstep], d = col[(size_t)(sl + 3) * sstep];
-                        sum += a;
-                        sum += b;
-                        sum += c;
-                        sum += d;
-                    }
-                    for (; sl < p.S; ++sl) sum += col[(size_t)sl * sstep];
-                    const int n = done_list[b0 + ti] * kTileRows + lane;
-                    if (n < p.N) p.y[(size_t)m * p.N + n] = sum;
-                }
-                __syncthreads();  // the stage is refilled by the next batch
-            }
-        }
-    }
-}
-
 // Split-K across a cluster.  The cluster's tiles [ta, tb) are dealt round
 // robin to its S CTAs: local tile lt belongs to CTA lt % S, slot lt / S.  Every
 // CTA stores each partial sum of its slice straight into the owner's shared
@@ -499,8 +412,6 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
     unsigned char* lut = smem;
     float* tbuf = reinterpret_cast<float*>(smem + kLutBytes);
     float* xs = tbuf + 16 * kPad;
-    int* done_list = reinterpret_cast<int*>(xs + kSlice + kSlice / 32);  // [kMaxList]
-    int* done_count = done_list + kMaxList;
     unsigned char* lut2 = smem + kLut2Off;  // second token's table (M >= 2)
     float* pbuf = reinterpret_cast<float*>(smem + (p.M >= 2 ? kPbufOff2 : kPbufOff));  // cluster split-K only
 
@@ -654,12 +565,39 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
                 if (!more) break;
             }
         }
-        if (p.cluster)
-            cluster_finish(p, ta, tb, rank, pbuf);
-        else
-            splitk_finish(p, ta, tb, npad, done_list, done_count, reinterpret_cast<float*>(lut));
+        if (p.cluster) cluster_finish(p, ta, tb, rank, pbuf);
     }
     if (!triggered) pdl_launch_dependents();
+}
+
+// Split-K outside a cluster: the sum of the GEMV's partials [S][M][T*32].
+// Thread i owns output (m, n) = (i / N, i % N) and adds its S partials in
+// slice order s = 0..S-1 (the order of the cluster path), 16 loads in flight.
+constexpr int kReduceThreads = 128;
+__global__ void __launch_bounds__(kReduceThreads)
+    bitlin_decode_reduce(const float* __restrict__ partials, float* __restrict__ y, int M, int N, int S,
+                         long long npad)
+{
+    // The successor may launch at once: it reads nothing this kernel writes
+    // before its own wait, which covers this whole grid.
+    pdl_launch_dependents();
+    pdl_wait();  // the GEMV's partials are complete and visible
+    const long long i = (long long)blockIdx.x * kReduceThreads + threadIdx.x;
+    if (i >= (long long)M * N) return;
+    const int m = (int)(i / N), n = (int)(i - (long long)m * N);
+    const float* src = partials + (size_t)m * npad + n;
+    const size_t step = (size_t)M * npad;
+    float sum = 0.f;
+    for (int s0 = 0; s0 < S; s0 += 16) {
+        const int cnt = min(16, S - s0);
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = j < cnt ? __ldcg(src + (size_t)(s0 + j) * step) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (j < cnt) sum += v[j];
+    }
+    y[(size_t)m * N + n] = sum;
 }
 
 }  // namespace
@@ -706,24 +644,34 @@ int max_clusters(int S, int num_sms)
 
 }  // namespace
 
-cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_t s)
+namespace {
+
+cudaError_t configure_decode()
 {
     static bool configured = false;
-    if (!configured) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess && g_max_smem < kPbufOff2) e = cudaErrorInvalidConfiguration;
-        for (auto k : {bitlin_decode_gemv<false>, bitlin_decode_gemv<true>}) {
-            if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g_max_smem);
-            if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        }
-        if (e != cudaSuccess) return e;
-        configured = true;
+    if (configured) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess && g_max_smem < kPbufOff2) e = cudaErrorInvalidConfiguration;
+    for (auto k : {bitlin_decode_gemv<false>, bitlin_decode_gemv<true>}) {
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g_max_smem);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     }
-    DecodeParams q = p;
-    const int base_smem = p.M >= 2 ? kPbufOff2 : kDecodeSmem;  // two tables from M = 2
-    int grid, smem = base_smem, cluster = 0;
+    if (e == cudaSuccess) configured = true;
+    return e;
+}
+
+// Launch shape of one call: the grid, its shared memory, the cluster size (0 =
+// split-K through the scratch and bitlin_decode_reduce), and q's launcher fields.
+struct DecodeShape {
+    int grid, smem, cluster;
+};
+
+DecodeShape decode_shape(const DecodeParams& p, int num_sms, DecodeParams& q)
+{
+    q = p;
+    DecodeShape d{0, p.M >= 2 ? kPbufOff2 : kDecodeSmem, 0};  // two tables from M = 2
     q.cluster = 0;
     // Split-K across a cluster when the slices fit one (S <= 16) and the
     // partial sums fit shared memory; else through the global scratch.
@@ -737,22 +685,43 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
             if (pb <= kPbufBytes && poff + pb <= g_max_smem) {
                 q.cluster = 1;
                 q.ctas_per_slice = ncl;
-                grid = p.S * ncl;
-                smem = poff + (int)pb;
-                cluster = p.S;
+                d.grid = p.S * ncl;
+                d.smem = poff + (int)pb;
+                d.cluster = p.S;
             }
         }
     }
     if (!q.cluster) {
         if (p.S <= num_sms) {
             q.ctas_per_slice = num_sms / p.S < p.T ? num_sms / p.S : p.T;
-            grid = p.S * q.ctas_per_slice;
+            d.grid = p.S * q.ctas_per_slice;
         } else {
             const long long U = (long long)p.S * p.T;
             q.ctas_per_slice = 0;
-            grid = (int)(U < num_sms ? U : num_sms);
+            d.grid = (int)(U < num_sms ? U : num_sms);
         }
     }
+    return d;
+}
+
+}  // namespace
+
+cudaError_t bitlin_decode_kernels(const DecodeParams& p, int num_sms, int* kernels)
+{
+    cudaError_t e = configure_decode();
+    if (e != cudaSuccess) return e;
+    DecodeParams q;
+    *kernels = decode_shape(p, num_sms, q).cluster ? 1 : 2;
+    return cudaSuccess;
+}
+
+cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_t s)
+{
+    cudaError_t e = configure_decode();
+    if (e != cudaSuccess) return e;
+    DecodeParams q;
+    const DecodeShape d = decode_shape(p, num_sms, q);
+    const int grid = d.grid, smem = d.smem, cluster = d.cluster;
 
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -769,6 +738,17 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = cluster ? 2 : 1;
-    return p.M >= 2 ? cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<true>, q)
-                    : cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<false>, q);
+    e = p.M >= 2 ? cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<true>, q)
+                 : cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<false>, q);
+    if (e != cudaSuccess || q.cluster) return e;
+    // Scratch split-K: the sum over the slices, launched as the GEMV's dependent.
+    const long long outs = (long long)p.M * p.N;
+    cudaLaunchConfig_t rc = {};
+    rc.gridDim = dim3((unsigned)((outs + kReduceThreads - 1) / kReduceThreads));
+    rc.blockDim = dim3(kReduceThreads);
+    rc.stream = s;
+    rc.attrs = attr;
+    rc.numAttrs = 1;
+    return cudaLaunchKernelEx(&rc, bitlin_decode_reduce, static_cast<const float*>(p.partials), p.y, p.M, p.N,
+                              p.S, (long long)p.T * kTileRows);
 }

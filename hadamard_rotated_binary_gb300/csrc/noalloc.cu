@@ -16,10 +16,9 @@
 // device, with that device current, looks the address up with
 // cudaGetSymbolAddress and caches it; make that first call before any stream
 // capture.  All calls share the array and it keeps the previous call's
-// contents: every call clears the split-K tickets it uses (cudaMemsetAsync on
-// its stream) before launching; the partial sums need no clearing, each call
-// writes all of them before they are read.  Two calls whose kernels overlap
-// on the GPU (different streams, or concurrent host threads) race on it.
+// contents; nothing in it needs clearing: each call writes all the partial
+// sums it reads.  Two calls whose kernels overlap on the GPU (different
+// streams, or concurrent host threads) race on it.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -63,11 +62,9 @@ extern "C" bitlin_status bitlin_forward_noalloc(bitlin_t h, const float* x, int 
     if (!h || !x || !y || M < 1) return BITLIN_EINVAL;
     if (h->sticky != BITLIN_OK) return h->sticky;
 
-    // Scratch layout: tickets [T * kTicketStride] u32, then partials [S][M][T*32] f32.
-    const size_t ticket_bytes = (size_t)h->T * kTicketStride * sizeof(unsigned);
-    const size_t partial_off = (ticket_bytes + 255) & ~(size_t)255;
+    // Scratch layout: the split-K partials [S][M][T*32] f32.
     const size_t partial_bytes = (size_t)h->S * (size_t)M * h->T * kTileRows * sizeof(float);
-    if (partial_off + partial_bytes > kNoallocScratchBytes) return BITLIN_ESCRATCH;
+    if (partial_bytes > kNoallocScratchBytes) return BITLIN_ESCRATCH;
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -80,16 +77,14 @@ extern "C" bitlin_status bitlin_forward_noalloc(bitlin_t h, const float* x, int 
     e = scratch_address(dev, &base);
     if (e == cudaSuccess) {
         cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-        e = cudaMemsetAsync(base, 0, ticket_bytes, s);
-        if (e == cudaSuccess) {
+        {
             DecodeParams p;
             p.bits = h->dbits;
             p.scales = h->dscales;
             p.signs = h->signs;
             p.x = x;
             p.y = y;
-            p.counters = static_cast<unsigned*>(base);
-            p.partials = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + partial_off);
+            p.partials = static_cast<float*>(base);
             p.M = M;
             p.N = h->N;
             p.K = h->K;

@@ -138,16 +138,16 @@ bitlin_status bitlin_forward_host(bitlin_t h, const float* x_host, int M, float*
  * split-K scratch is a fixed array of bitlin_noalloc_scratch_bytes() bytes
  * (16 MiB) compiled into the library, which every GPU that loads the library
  * keeps until the process exits.  The call needs
- *     align256(ceil(N/32) * 128) + (K/512) * M * ceil(N/32) * 128  bytes
+ *     (K/512) * M * ceil(N/32) * 128  bytes
  * of it and returns BITLIN_ESCRATCH, launching nothing, when that exceeds the
  * array (for example M=1 fits up to N = 248,320 at K = 5120).
  * The first call on a device, with that device current, looks up the array's
  * device address (cudaGetSymbolAddress) and caches it: make that first call
  * before any stream capture.  Every call shares the array, which keeps the
- * previous call's contents; each call clears the part that must start at zero
- * (its split-K tickets) with cudaMemsetAsync on `stream`.  Calls whose kernels
- * overlap on the GPU (different streams, or several host threads) race on the
- * array: serialize them.
+ * previous call's contents (nothing in it needs clearing: each call writes
+ * every partial sum it reads).  Calls whose kernels overlap on the GPU
+ * (different streams, or several host threads) race on the array: serialize
+ * them.
  * Errors: BITLIN_EINVAL (NULL handle/x/y, M < 1, current device differs from
  * the handle's), BITLIN_ESCRATCH, BITLIN_ECUDA, and the handle's sticky error.
  */
@@ -235,6 +235,17 @@ size_t bitlin_noalloc_scratch_bytes(void);
 
 /* Select the path used for later calls (BITLIN_PATH_*).  EINVAL on an unknown value. */
 bitlin_status bitlin_set_path(bitlin_t h, int path);
+
+/*
+ * The plan of a bitlin_forward call with M tokens on this handle, without
+ * running it: *path = the BITLIN_PATH_* it takes (never AUTO), *kernels = the
+ * kernels it launches (decode: 1 when the split-K sums inside a thread-block
+ * cluster, 2 when a second kernel sums the partials; tensor paths: 2, the
+ * rotation and the GEMM).  The first call may set up the decode kernels'
+ * attributes on the current device.  Errors: BITLIN_EINVAL (NULL argument,
+ * M < 1), BITLIN_ECUDA.
+ */
+bitlin_status bitlin_plan(bitlin_t h, int M, int* path, int* kernels);
 
 /* Longest time, in nanoseconds, that any one wait inside the tensor-core
  * kernel may take before the kernel gives up and records BITLIN_ETIMEOUT

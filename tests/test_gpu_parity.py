@@ -307,6 +307,18 @@ def test_auto_path_choice(hrb):
         assert max_rel_l2(y[:, rows], ref[:m]) <= tol, m
 
 
+def test_plan_reports_path_and_kernels(hrb):
+    """bitlin_plan: the path of each M range, one kernel for the cluster split-K (10 slices at
+    K = 5120), two (GEMV + sum) for 34 slices at K = 17408, two (rotation + GEMM) on the tensor
+    paths; a forced path is reported as forced."""
+    gate = make_layer(hrb, *inputs("ffn_gate", 1)[1:4], 0)
+    down = make_layer(hrb, *inputs("ffn_down", 1)[1:4], 0)
+    assert [gate.plan(m) for m in (1, 2, 4, 5, 63, 64)] == [(1, 1), (1, 1), (1, 1), (3, 2), (3, 2), (2, 2)]
+    assert down.plan(1) == (1, 2)
+    gate.set_path(1)
+    assert gate.plan(200) == (1, 2)  # 200 tokens' partials do not fit shared memory: scratch + sum
+
+
 # ------------------------------------------------------------------ MLP block (gate|up -> SiLU -> down)
 
 def _mlp_pair(hrb, F, H, seed):
@@ -319,8 +331,8 @@ def _mlp_pair(hrb, F, H, seed):
 
 @pytest.mark.parametrize("M", [1, 4])
 def test_mlp_block_full_size(hrb, M):
-    """Bonsai-27B MLP shapes (5120 -> 2 x 17408 -> 5120): M = 1 on the decode GEMVs, M = 4 on
-    the exact tensor path, every output, <= 1e-5."""
+    """Bonsai-27B MLP shapes (5120 -> 2 x 17408 -> 5120) on the decode GEMVs (M = 1: one token
+    per pass; M = 4: two), every output, <= 1e-5."""
     gu, dn, lgu, ldn = _mlp_pair(hrb, 17408, 5120, 0xB1711A00 + 5)
     x = synth.random_x(0xB1711A00 + 5, M, 5120)
     y = hrb.mlp_forward(lgu, ldn, torch.from_numpy(x).cuda())
