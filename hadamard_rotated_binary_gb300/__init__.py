@@ -33,13 +33,17 @@ from ._binding import (  # noqa: F401
     header_functions,
     lib,
     library_path,
+    load_q1g128,
     mlp_forward,
+    q1g128_words,
 )
 
 __all__ = [
     "BitLinear",
     "BitlinError",
     "mlp_forward",
+    "load_q1g128",
+    "q1g128_words",
     "lib",
     "library_path",
     "header_functions",

@@ -60,6 +60,7 @@ def lib() -> ctypes.CDLL:
     L = ctypes.CDLL(path)
     P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
     L.bitlin_create.argtypes = [ctypes.POINTER(P), i32, i32, P, P, P, i32]
+    L.bitlin_create_q1g128.argtypes = [ctypes.POINTER(P), i32, i32, P, P, i32]
     L.bitlin_forward.argtypes = [P, P, i32, P, P]
     L.bitlin_forward_host.argtypes = [P, P, i32, P, P]
     L.bitlin_forward_noalloc.argtypes = [P, P, i32, P, P]
@@ -77,7 +78,7 @@ def lib() -> ctypes.CDLL:
     L.bitlin_cuda_error.argtypes = [P]
     L.bitlin_status_string.argtypes = [i32]
     L.bitlin_status_string.restype = ctypes.c_char_p
-    for name in ("bitlin_create", "bitlin_forward", "bitlin_forward_host", "bitlin_embed", "bitlin_mlp_forward",
+    for name in ("bitlin_create", "bitlin_create_q1g128", "bitlin_forward", "bitlin_forward_host", "bitlin_embed", "bitlin_mlp_forward",
                  "bitlin_argmax", "bitlin_set_path", "bitlin_plan", "bitlin_set_wait_budget", "bitlin_test_stall", "bitlin_destroy", "bitlin_get_error",
                  "bitlin_cuda_error", "bitlin_version"):
         getattr(L, name).restype = i32
@@ -109,6 +110,26 @@ def mlp_forward(gate_up: "BitLinear", down: "BitLinear", x, out=None, stream=Non
     return out
 
 
+def q1g128_words(N: int, K: int) -> int:
+    """32-bit words of one stored Q1G128 tensor: N*K/256 of scales, then N*K/32 of bits."""
+    if N < 1 or K < 1024 or K % 1024:
+        raise ValueError("N >= 1 and K a positive multiple of 1024")
+    return N * K // 256 + N * K // 32
+
+
+def load_q1g128(path: str, N: int, K: int, offset: int = 0, device="cuda"):
+    """Read one stored Q1G128 tensor (q1g128_words(N, K) little-endian words starting at byte
+    `offset` of the file) into a CUDA int32 tensor for BitLinear.from_q1g128."""
+    import numpy as np
+    import torch
+
+    n = q1g128_words(N, K)
+    words = np.fromfile(path, dtype="<u4", count=n, offset=offset)
+    if words.size != n:
+        raise ValueError(f"{path}: {4 * words.size} bytes at offset {offset}, need {4 * n}")
+    return torch.from_numpy(words.view(np.int32)).to(device)
+
+
 class BitLinear:
     """One folded 1-bit matrix on the GPU (a bitlin handle).
 
@@ -121,7 +142,6 @@ class BitLinear:
     def __init__(self, bits, scales, signs, perm: int = PERM_NONE):
         import torch
 
-        L = lib()
         N = int(bits.shape[0])
         K = int(bits.shape[1]) * 32
         for t in (bits, scales, signs):
@@ -131,13 +151,39 @@ class BitLinear:
             raise ValueError("signs must be float32")
         h = ctypes.c_void_p()
         with torch.cuda.device(bits.device):
-            st = L.bitlin_create(ctypes.byref(h), N, K, bits.data_ptr(), scales.data_ptr(),
-                                 signs.data_ptr(), int(perm))
+            st = lib().bitlin_create(ctypes.byref(h), N, K, bits.data_ptr(), scales.data_ptr(),
+                                     signs.data_ptr(), int(perm))
         if st != BITLIN_OK:
             raise BitlinError(st, "bitlin_create")
+        self._adopt(h, N, K, perm, bits.device)
+
+    def _adopt(self, h, N: int, K: int, perm: int, device):
         self._h = h
         self.N, self.K, self.perm = N, K, perm
-        self.device = bits.device
+        self.device = device
+
+    @classmethod
+    def from_q1g128(cls, qdata, N: int, K: int, signs, perm: int = PERM_NONE) -> "BitLinear":
+        """bitlin_create_q1g128: a handle from one Q1G128 tensor in its stored form (fp16 scales
+        two per word, then the sign bits; q1g128_words(N, K) words in a CUDA tensor)."""
+        import torch
+
+        for t in (qdata, signs):
+            if not (t.is_cuda and t.is_contiguous()):
+                raise ValueError("qdata and signs must be contiguous CUDA tensors")
+        if qdata.numel() * qdata.element_size() != 4 * q1g128_words(N, K):
+            raise ValueError(f"qdata must hold {4 * q1g128_words(N, K)} bytes for N={N}, K={K}")
+        if signs.dtype != torch.float32:
+            raise ValueError("signs must be float32")
+        h = ctypes.c_void_p()
+        with torch.cuda.device(qdata.device):
+            st = lib().bitlin_create_q1g128(ctypes.byref(h), int(N), int(K), qdata.data_ptr(), signs.data_ptr(),
+                                            int(perm))
+        if st != BITLIN_OK:
+            raise BitlinError(st, "bitlin_create_q1g128")
+        self = cls.__new__(cls)
+        self._adopt(h, int(N), int(K), perm, qdata.device)
+        return self
 
     @property
     def handle(self) -> ctypes.c_void_p:

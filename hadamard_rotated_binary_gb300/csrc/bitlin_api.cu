@@ -286,6 +286,23 @@ fail:
     return status;
 }
 
+// A Q1G128 tensor as the engine stores it: the fp16 scales (two per word,
+// index n*(K/128) + g, the even index in the low half) and then the bits, in
+// one array of words ("Inside the One-Bit Engine", embedding station).  The
+// scales take N*K/256 words; on a little-endian device the low half of a word
+// is the 16-bit element at the lower address, so that prefix is the [N][K/128]
+// binary16 array bitlin_create takes.
+bitlin_status bitlin_create_q1g128(bitlin_t* out, int N, int K, const uint32_t* qdata, const float* signs,
+                                   int perm_flag)
+{
+    if (!out) return BITLIN_EINVAL;
+    *out = nullptr;
+    if (!qdata || N < 1 || K < 1024 || K % 1024 != 0) return BITLIN_EINVAL;
+    const size_t scale_words = (size_t)N * (size_t)(K / 256);
+    return bitlin_create(out, N, K, qdata + scale_words, reinterpret_cast<const uint16_t*>(qdata), signs,
+                         perm_flag);
+}
+
 bitlin_status bitlin_set_path(bitlin_t h, int path)
 {
     if (!h || path < BITLIN_PATH_AUTO || path > BITLIN_PATH_TC_EXACT) return BITLIN_EINVAL;

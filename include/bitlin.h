@@ -97,6 +97,27 @@ bitlin_status bitlin_create(bitlin_t* out, int N, int K, const uint32_t* packed_
                             const uint16_t* scales, const float* signs, int perm_flag);
 
 /*
+ * bitlin_create from one Q1G128 tensor in its stored form: a single array of
+ * 32-bit words holding first every fp16 scale, two per word, then every sign
+ * bit.  Layout ("Inside the One-Bit Engine", embedding-lookup station, and
+ * its weight-format station):
+ *     scale of row n, group g (sidx = n*(K/128) + g): half (sidx & 1) of word
+ *         sidx >> 1, the even index in the low 16 bits;
+ *     scale_words = N*K/256 (every row has K/128 scales, a multiple of 8);
+ *     bit k of row n: bit (k & 31) of word scale_words + n*(K/32) + (k >> 5),
+ *         1 means +1, 0 means -1.
+ * The whole array is N*K*9/256 words: 720 bytes per row at K = 5120 (the
+ * 248,320 x 5120 vocabulary matrix: 178,790,400 bytes).
+ *
+ *   qdata  device pointer to that array, 16-byte aligned (the bits then are
+ *          too: scale_words*4 is a multiple of 16).
+ * Everything else, including ownership (the array may be freed after the
+ * call) and the errors, is as bitlin_create.
+ */
+bitlin_status bitlin_create_q1g128(bitlin_t* out, int N, int K, const uint32_t* qdata, const float* signs,
+                                   int perm_flag);
+
+/*
  * y[M][N] = the folded product of x[M][K] (see the top of this file).
  *
  *   x       device pointer, float [M][K], row-major, read only.

@@ -154,6 +154,21 @@ def dequant_row(bits: np.ndarray, scales: np.ndarray, n: int) -> np.ndarray:
     return out
 
 
+def q1g128_weight(qdata: np.ndarray, N: int, K: int, n: int, k: int) -> float:
+    """Weight (n, k) read from one stored Q1G128 tensor by the engine page's indexing
+    ("Inside the One-Bit Engine", embedding-lookup and weight-format stations): scale index
+    sidx = n*(K/128) + (k >> 7) selects half (sidx & 1) of word sidx >> 1 (two binary16 per
+    word, the first in the low 16 bits); the bit words start after the scale words (N*K/256
+    of them), row n at n*(K/32), weight k at bit k & 31 of word k >> 5; w = (2*bit - 1) * scale."""
+    G = K // 128
+    scale_words = N * G // 2
+    sidx = n * G + (k >> 7)
+    half = (int(qdata[sidx >> 1]) >> (16 * (sidx & 1))) & 0xFFFF
+    word = int(qdata[scale_words + n * (K >> 5) + (k >> 5)])
+    bit = (word >> (k & 31)) & 1
+    return (2.0 * bit - 1.0) * f16_to_f64(half)
+
+
 def silu(g: np.ndarray) -> np.ndarray:
     """SiLU(g) = g / (1 + e^-g), f64 ("Inside the One-Bit Engine", MLP station)."""
     g = np.asarray(g, dtype=np.float64)

@@ -164,3 +164,16 @@ def sample_rows(seed: int, N: int, count: int) -> np.ndarray:
     r = np.unique((stream(seed, 99, 4 * count) % np.uint64(N)).astype(np.int64))
     r = r[(r != 0) & (r != N - 1)][: count - 2]
     return np.unique(np.concatenate([[0, N - 1], r]).astype(np.int64))
+
+
+def q1g128_blob(bits: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """The same weights in the stored Q1G128 form of the "Inside the One-Bit Engine" page
+    (embedding-lookup station): one uint32 array holding first the fp16 scales, two per word
+    (scale index n*(K/128) + g; the even index in the low 16 bits), then the bit words
+    [N][K/32].  Layout only; N*K/256 + N*K/32 words."""
+    s = np.ascontiguousarray(scales, dtype=np.uint16).reshape(-1).astype(np.uint32)
+    if s.size % 2:
+        raise ValueError("an even number of scales (K is a multiple of 1024)")
+    words = s[0::2] | (s[1::2] << np.uint32(16))
+    return np.concatenate([words, np.ascontiguousarray(bits, dtype=np.uint32).reshape(-1)])
+

@@ -51,6 +51,10 @@ def test_argument_validation_without_device(L):
     assert L.bitlin_argmax(None, p, 1, None, p, None) == hrb.BITLIN_EINVAL
     assert L.bitlin_mlp_forward(None, None, p, 1, p, None) == hrb.BITLIN_EINVAL
     assert L.bitlin_set_path(None, 0) == hrb.BITLIN_EINVAL
+    assert L.bitlin_create_q1g128(None, 8, 1024, p, p, 0) == hrb.BITLIN_EINVAL
+    assert L.bitlin_create_q1g128(ctypes.byref(h), 8, 1024, None, p, 0) == hrb.BITLIN_EINVAL
+    assert L.bitlin_create_q1g128(ctypes.byref(h), 8, 1000, p, p, 0) == hrb.BITLIN_EINVAL
+    assert h.value is None
     a, b = ctypes.c_int32(), ctypes.c_int32()
     assert L.bitlin_plan(None, 1, ctypes.byref(a), ctypes.byref(b)) == hrb.BITLIN_EINVAL
     assert L.bitlin_get_error(None) == hrb.BITLIN_EINVAL

@@ -503,3 +503,38 @@ def test_bounded_wait_times_out_without_hanging(hrb):
     fresh = make_layer(hrb, bits, scales, signs, 0)
     y = run(fresh, x)
     assert max_rel_l2(y, oracle.forward(bits, scales, signs, 0, x)) <= DECODE_TOL
+
+
+# ------------------------------------------------------------------ the stored Q1G128 form
+
+@pytest.mark.parametrize("name", ["attn_kv", "ssm_out"])
+def test_q1g128_stored_form_handle(hrb, tmp_path, name):
+    """A handle made from the stored Q1G128 tensor (read from a file at a byte offset) gives
+    the same y, bit for bit, as one made from separate bits and scales, within 1e-5 of the
+    oracle; its embedding rows match the oracle's."""
+    w, bits, scales, signs, x = inputs(name, 3)
+    blob = synth.q1g128_blob(bits, scales)
+    path = tmp_path / "tensor.bin"
+    with open(path, "wb") as f:
+        f.write(b"\0" * 64)  # something in front of the tensor, as in a checkpoint file
+        f.write(blob.astype("<u4").tobytes())
+    qd = hrb.load_q1g128(str(path), w.N, w.K, offset=64)
+    tg = torch.from_numpy(signs).cuda()
+    from_blob = hrb.BitLinear.from_q1g128(qd, w.N, w.K, tg, w.perm)
+    del qd  # the handle owns its copy
+    plain = make_layer(hrb, bits, scales, signs, w.perm)
+    xd = torch.from_numpy(x).cuda()
+    y1, y2 = from_blob(xd), plain(xd)
+    torch.cuda.synchronize()
+    assert from_blob.get_error() == 0
+    assert torch.equal(y1, y2)
+    ref = oracle.forward(bits, scales, signs, w.perm, x)
+    assert max_rel_l2(y1.cpu().numpy().astype(np.float64), ref) <= DECODE_TOL
+    ids = [0, w.N // 2, w.N - 1]
+    h = from_blob.embed(torch.tensor(ids, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    # (the permutation flag does not apply to embedding rows)
+    assert max_rel_l2(h.cpu().numpy().astype(np.float64), oracle.embed(bits, scales, signs, ids)) <= DECODE_TOL
+    with pytest.raises(ValueError):
+        hrb.BitLinear.from_q1g128(torch.zeros(5, dtype=torch.int32, device="cuda"), w.N, w.K, tg, w.perm)
+

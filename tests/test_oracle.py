@@ -328,3 +328,57 @@ def test_embedding_closed_form_and_brute_force(oracle_lib):
     got = oracle_lib.embed(bits, scales, signs, [0, 3, 1])
     ref = (Hb @ Wd[[0, 3, 1]].T).T * signs.astype(np.float64)[None, :]
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------------------------------ NEXT row: the stored Q1G128 form
+
+def _dense_weights(bits, scales):
+    """w[n][k] = (2 bit - 1) * scale through numpy's own bit unpacking and fp16 decoding."""
+    N, W = bits.shape
+    pm = np.unpackbits(np.ascontiguousarray(bits).view(np.uint8), bitorder="little").reshape(N, 32 * W)
+    sc = np.repeat(np.ascontiguousarray(scales).view(np.float16).astype(np.float64), 128, axis=1)
+    return (2.0 * pm - 1.0) * sc
+
+
+def test_q1g128_stored_form_size_matches_page_figures():
+    """One row is 720 bytes at K = 5120 and the vocabulary tensor 178,790,400 bytes."""
+    from hadamard_rotated_binary_gb300 import q1g128_words
+
+    f = _page_facts()
+    K, N = 5120, 3
+    blob = synth.q1g128_blob(synth.random_bits(5, N, K), synth.random_scales(5, N, K, 0.01, 0.02))
+    assert blob.dtype == np.uint32 and 4 * blob.size == N * int(f["row_bytes_k5120"])
+    assert 4 * q1g128_words(int(f["token_embd_rows"]), K) == int(f["token_embd_bytes"])
+    assert 4 * q1g128_words(N, K) == 4 * blob.size
+
+
+def test_q1g128_reader_follows_the_page_indexing(oracle_lib):
+    """A hand-made tensor: scales 1..8 (one row, K = 1024), bit word 0 = 0b101.  Scale index 0
+    sits in the low half of word 0 (unpack2x16float's first component is bits 0..15), and the bit
+    words start right after the N*K/256 scale words."""
+    K, N = 1024, 1
+    scales = np.array([[np.float16(v).view(np.uint16) for v in range(1, 9)]], dtype=np.uint16)
+    bits = np.zeros((N, K // 32), dtype=np.uint32)
+    bits[0, 0] = 0b101
+    bits[0, 31] = 0x80000000  # the last weight of the row
+    blob = synth.q1g128_blob(bits, scales)
+    assert blob[0] == 0x40003C00 and blob.size == 4 + 32  # 2.0 high, 1.0 low; 4 scale words
+    got = [oracle_lib.q1g128_weight(blob, N, K, 0, k) for k in (0, 1, 2, 127, 128, 1023)]
+    assert got == [1.0, -1.0, 1.0, -1.0, -2.0, 8.0]
+
+
+def test_q1g128_reader_against_numpy_dequantization(oracle_lib):
+    """Every weight of a random 3 x 2048 tensor read from the stored form equals numpy's own
+    unpacking; a packer with the two halves of each scale word swapped fails (negative control)."""
+    N, K = 3, 2048
+    bits = synth.random_bits(11, N, K)
+    scales = synth.random_scales(11, N, K, 0.01, 0.05)
+    dense = _dense_weights(bits, scales)
+    blob = synth.q1g128_blob(bits, scales)
+    got = np.array([[oracle_lib.q1g128_weight(blob, N, K, n, k) for k in range(K)] for n in range(N)])
+    np.testing.assert_array_equal(got, dense)
+    s = scales.reshape(-1).astype(np.uint32)
+    swapped = np.concatenate([s[1::2] | (s[0::2] << np.uint32(16)), bits.reshape(-1)])
+    bad = np.array([oracle_lib.q1g128_weight(swapped, N, K, 0, k) for k in range(0, K, 128)])
+    assert not np.array_equal(bad, dense[0, ::128])
+
