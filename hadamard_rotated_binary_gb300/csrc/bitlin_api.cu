@@ -204,6 +204,11 @@ bitlin_status bitlin_create(bitlin_t* out, int N, int K, const uint32_t* packed_
     if (!h) return BITLIN_ENOMEM;
     h->device = dev;
     h->num_sms = sms;
+    if (cudaDeviceGetAttribute(&h->host_page_tables, cudaDevAttrPageableMemoryAccessUsesHostPageTables, dev) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        h->host_page_tables = 0;
+    }
     h->N = N;
     h->K = K;
     h->perm = perm_flag;
@@ -382,6 +387,22 @@ bitlin_status bitlin_mlp_forward(bitlin_t gate_up, bitlin_t down, const float* x
     return run_path(down, down->mlp_in, M, y, s, 1);
 }
 
+// Address under which the kernels may use a host buffer directly, or nullptr
+// when it has to be staged through device memory: page-locked memory mapped
+// into the device's address space (its device pointer), or any host memory on
+// a device that reads pageable memory through the host's page tables.
+static const void* host_direct(bitlin_t h, const void* p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+    if (a.type == cudaMemoryTypeUnregistered && h->host_page_tables) return p;
+    return nullptr;
+}
+
 bitlin_status bitlin_forward_host(bitlin_t h, const float* x_host, int M, float* y_host,
                                   bitlin_stream_t stream)
 {
@@ -389,7 +410,11 @@ bitlin_status bitlin_forward_host(bitlin_t h, const float* x_host, int M, float*
     if (h->sticky != BITLIN_OK) return h->sticky;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (!h->hx || h->h_M < M) {
+    // The kernels read x and write y in host memory where the device can reach
+    // it (no copy operations); otherwise x and y pass through device buffers.
+    const float* xd = static_cast<const float*>(host_direct(h, x_host));
+    float* yd = static_cast<float*>(const_cast<void*>(host_direct(h, y_host)));
+    if ((!xd || !yd) && (!h->hx || h->h_M < M)) {
         free_dev(h->hx);
         free_dev(h->hy);
         h->h_M = 0;
@@ -398,15 +423,22 @@ bitlin_status bitlin_forward_host(bitlin_t h, const float* x_host, int M, float*
         if (e != cudaSuccess) return from_cuda(h, e);
         h->h_M = M;
     }
-    e = cudaMemcpyAsync(h->hx, x_host, (size_t)M * h->K * sizeof(float), cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return from_cuda(h, e);
-    bitlin_status st = bitlin_forward(h, h->hx, M, h->hy, stream);
+    if (!xd) {
+        e = cudaMemcpyAsync(h->hx, x_host, (size_t)M * h->K * sizeof(float), cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return from_cuda(h, e);
+        xd = h->hx;
+    }
+    bitlin_status st = bitlin_forward(h, xd, M, yd ? yd : h->hy, stream);
     if (st != BITLIN_OK) return st;
-    e = cudaMemcpyAsync(y_host, h->hy, (size_t)M * h->N * sizeof(float), cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(h->h_err, h->dev_error, sizeof(int), cudaMemcpyDeviceToHost, s);
+    e = cudaSuccess;
+    if (!yd) e = cudaMemcpyAsync(y_host, h->hy, (size_t)M * h->N * sizeof(float), cudaMemcpyDeviceToHost, s);
+    // Only the tensor-core kernels can record a timeout (the decode GEMV has no
+    // waits of its own), so the error word is read back after those alone.
+    const bool tc = choose_path(h, M) != BITLIN_PATH_DECODE;
+    if (e == cudaSuccess && tc) e = cudaMemcpyAsync(h->h_err, h->dev_error, sizeof(int), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return from_cuda(h, e);
-    if (*h->h_err == kDevErrTimeout) h->sticky = BITLIN_ETIMEOUT;
+    if (tc && *h->h_err == kDevErrTimeout) h->sticky = BITLIN_ETIMEOUT;
     return h->sticky;
 }
 

@@ -91,6 +91,10 @@ struct bitlin {
     int* h_err = nullptr;      // pinned copy of the error word
     long long wait_budget_ns = 0;
     int stall_test = 0;
+    // The device reads pageable host memory coherently through the host's page
+    // tables (a hardware-coherent CPU-GPU link): bitlin_forward_host may then
+    // hand the caller's buffers to the kernels as they are.
+    int host_page_tables = 0;
 
     // MLP block (bitlin_mlp_forward on the down-projection handle): the gate and
     // up outputs [M][2K] that the down projection reads through SiLU

@@ -136,9 +136,18 @@ bitlin_status bitlin_create_q1g128(bitlin_t* out, int N, int K, const uint32_t* 
 bitlin_status bitlin_forward(bitlin_t h, const float* x, int M, float* y, bitlin_stream_t stream);
 
 /*
- * The same product with x and y in HOST memory: copies x to the device, runs
- * bitlin_forward on `stream`, copies y back and synchronizes the stream.
- * Pinned host buffers give the fastest copies; pageable memory also works.
+ * The same product with x and y in HOST memory; returns after the result is
+ * in y_host (the stream is synchronized).  How the data moves depends on the
+ * buffer and the device:
+ *   - page-locked memory mapped into the device's address space (for example
+ *     from cudaHostAlloc or cudaHostRegister), and any host memory on a device
+ *     that reads pageable memory through the host's page tables (a coherent
+ *     CPU-GPU link): the kernels read x and write y there directly, with no
+ *     copy operation;
+ *   - otherwise x is copied into a device buffer the handle keeps (allocated
+ *     on the first call with a new largest M), the product runs there, and y
+ *     is copied back.
+ * x_host must not change and y_host must not be read until the call returns.
  * Errors: as bitlin_forward, plus BITLIN_ETIMEOUT from this call's kernels.
  */
 bitlin_status bitlin_forward_host(bitlin_t h, const float* x_host, int M, float* y_host,

@@ -266,13 +266,24 @@ def test_cuda_graph_replay_matches(hrb):
     assert torch.equal(yd, eager)
 
 
-def test_forward_host_buffers(hrb):
-    w, bits, scales, signs, x = inputs("ssm_out")
+@pytest.mark.parametrize("name,M", [("ssm_out", 1), ("ffn_down", 2), ("attn_kv", 70)])
+def test_forward_host_buffers(hrb, name, M):
+    """Host buffers, pageable (numpy) and page-locked (torch pin_memory): the same y, bit for
+    bit, as the device-buffer call, within tolerance of the oracle; on the decode, scratch
+    split-K and bf16 tensor paths."""
+    w, bits, scales, signs, x = inputs(name, M)
     layer = make_layer(hrb, bits, scales, signs, w.perm)
-    y = np.empty((1, w.N), dtype=np.float32)
+    y_dev = layer(torch.from_numpy(x).cuda()).cpu().numpy()
+    y = np.full((M, w.N), np.nan, dtype=np.float32)
     layer.forward_host(x, y)
+    xp = torch.from_numpy(x).pin_memory()
+    yp = torch.full((M, w.N), float("nan")).pin_memory()
+    layer.forward_host(xp.numpy(), yp.numpy())
+    assert layer.get_error() == 0
+    np.testing.assert_array_equal(y, y_dev)
+    np.testing.assert_array_equal(yp.numpy(), y_dev)
     ref = oracle.forward(bits, scales, signs, w.perm, x)
-    assert max_rel_l2(y.astype(np.float64), ref) <= DECODE_TOL
+    assert max_rel_l2(y.astype(np.float64), ref) <= (DECODE_TOL if M < 64 else PREFILL_TOL)
 
 
 # ------------------------------------------------------------------ exact tensor path (2 <= M < 64)
@@ -500,6 +511,15 @@ def test_bounded_wait_times_out_without_hanging(hrb):
     with pytest.raises(hrb.BitlinError):
         layer(torch.from_numpy(x).cuda())
     layer.close()
+    # The host-buffer entry point reports the timeout of its own call.
+    stalled = make_layer(hrb, bits, scales, signs, 0)
+    stalled.set_path(hrb.PATH_PREFILL)
+    stalled.set_wait_budget(200_000_000)
+    stalled.test_stall(True)
+    with pytest.raises(hrb.BitlinError) as e:
+        stalled.forward_host(x, np.empty((1, w.N), dtype=np.float32))
+    assert e.value.status == hrb.BITLIN_ETIMEOUT
+    stalled.close()
     fresh = make_layer(hrb, bits, scales, signs, 0)
     y = run(fresh, x)
     assert max_rel_l2(y, oracle.forward(bits, scales, signs, 0, x)) <= DECODE_TOL
