@@ -7,11 +7,15 @@
 // (order: optional tiled->grouped permutation, x * signs, normalized
 // Sylvester-Walsh transform in blocks of 1024 scaled by 1/32).
 //
-// One warp per (token, block): lane q holds x[32p + q] for p = 0..31 in
-// registers (every load and store is a coalesced row of 32 elements).
-// H1024 = H32 (x) H32: 32-point butterflies across lanes (warp shuffles) for
-// each p, then 32-point butterflies across the 32 registers.  Memory-bound:
-// 4 bytes read and 2 written per element.
+// One warp per (token, block).  The 1024-point transform is separable over the
+// ten bits of the element index, so any placement of the elements on lanes and
+// registers works if each bit's butterflies pair the right values.  Vector
+// variant (x 16-byte aligned): element i = 128 p + 4 q + j (p < 8, j < 4)
+// sits in register 4p + j of lane q, so each lane reads 8 float4 and writes 8
+// groups of 4 bf16; bits 0-1 (j) and 7-9 (p) are butterflies across registers,
+// bits 2-6 (q) across lanes (warp shuffles).  Scalar variant (any alignment):
+// element i = 32 p + q in register p of lane q.  Memory-bound: 4 bytes read and
+// 2 written per element (4 x 2 in the exact mode).
 #include <cuda_bf16.h>
 
 #include "bitlin_internal.cuh"
@@ -25,71 +29,148 @@ __device__ __forceinline__ int perm_source(int k)
     return d + 128 * (kk + 16 * r);
 }
 
+// The rotated values of one (token, block), 32 per lane, written as bf16 (one
+// row) or as three digits and a zero row, one element at a time.  off(r) is
+// the block offset of register r of this lane.
+template <typename Off>
+__device__ __forceinline__ void store_rotated(const float (&v)[32], __nv_bfloat16* out, int K, int digits,
+                                              Off off)
+{
+    if (!digits) {
+#pragma unroll
+        for (int r = 0; r < 32; ++r) out[off(r)] = __float2bfloat16_rn(v[r] * 0.03125f);
+        return;
+    }
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        const float t = v[r] * 0.03125f;  // exact scaling by 1/32
+        const __nv_bfloat16 hi = __float2bfloat16_rn(t);
+        const float r1 = t - __bfloat162float(hi);  // exact
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const float r2 = r1 - __bfloat162float(mid);  // exact
+        const int k = off(r);
+        out[k] = hi;
+        out[(size_t)K + k] = mid;
+        out[2 * (size_t)K + k] = __float2bfloat16_rn(r2);
+        out[3 * (size_t)K + k] = __float2bfloat16_rn(0.f);
+    }
+}
+
+// The vector placement: registers 4p .. 4p+3 of lane q are the consecutive
+// elements 128 p + 4 q .. + 3, stored as one 8-byte group per row.
+__device__ __forceinline__ uint2 pack4(float a, float b, float c, float d)
+{
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+
+__device__ __forceinline__ void store_rotated_vec(const float (&v)[32], __nv_bfloat16* out, int K, int digits,
+                                                  int lane)
+{
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        float t[4], d1[4], d2[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            t[j] = v[4 * p + j] * 0.03125f;  // exact scaling by 1/32
+            d1[j] = t[j] - __bfloat162float(__float2bfloat16_rn(t[j]));  // exact
+            d2[j] = d1[j] - __bfloat162float(__float2bfloat16_rn(d1[j]));  // exact
+        }
+        uint2* o = reinterpret_cast<uint2*>(out + 128 * p + 4 * lane);
+        o[0] = pack4(t[0], t[1], t[2], t[3]);  // bf16(t): the row, or the hi digit
+        if (digits) {
+            o[K / 4] = pack4(d1[0], d1[1], d1[2], d1[3]);      // mid = bf16(t - hi)
+            o[K / 2] = pack4(d2[0], d2[1], d2[2], d2[3]);      // lo = bf16(t - hi - mid)
+            o[3 * (K / 4)] = make_uint2(0u, 0u);                // zero row
+        }
+    }
+}
+
+__device__ __forceinline__ float silu_times(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+// VEC: element i = 128 p + 4 q + j in register 4p + j of lane q (x 16-byte
+// aligned); otherwise element i = 32 p + q in register p.  SWIGLU: x is
+// [M][2K] gate | up and the input is silu(gate) * up, SiLU(g) = g / (1 + e^-g)
+// in f32 ("Inside the One-Bit Engine", MLP station).
+template <bool VEC, bool SWIGLU>
 __global__ void __launch_bounds__(256) bitlin_rotate_bf16(const float* __restrict__ x,
-                                                          const float* __restrict__ signs, int M,
-                                                          int K, int perm, int digits, int swiglu,
-                                                          __nv_bfloat16* __restrict__ xt)
+                                                          const float* __restrict__ signs, int M, int K,
+                                                          int perm, int digits, __nv_bfloat16* __restrict__ xt)
 {
     const int lane = threadIdx.x & 31;
     const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int B = K / 1024;
     if (gw >= (long long)M * B) return;
     const int m = (int)(gw / B), b = (int)(gw - (long long)m * B);
-    // With swiglu set, x is [M][2K] gate | up and the input is silu(gate) * up,
-    // SiLU(g) = g / (1 + e^-g) in f32 ("Inside the One-Bit Engine", MLP station).
-    const float* xm = x + (size_t)m * (swiglu ? 2 * K : K);
-
+    const float* xm = x + (size_t)m * (SWIGLU ? 2 * K : K);
     float v[32];
+    if (VEC) {
 #pragma unroll
-    for (int p = 0; p < 32; ++p) {
-        const int k = b * 1024 + 32 * p + lane;
-        const int src = perm ? perm_source(k) : k;
-        float a = __ldg(xm + src);
-        if (swiglu) {
-            const float u = __ldg(xm + K + src);
-            a = a / (1.f + expf(-a)) * u;
+        for (int p = 0; p < 8; ++p) {
+            const int k = b * 1024 + 128 * p + 4 * lane;
+            const int src = perm ? perm_source(k) : k;  // heads move whole: src stays a multiple of 4
+            float4 a = __ldg(reinterpret_cast<const float4*>(xm + src));
+            if (SWIGLU) {
+                const float4 u = __ldg(reinterpret_cast<const float4*>(xm + K + src));
+                a = make_float4(silu_times(a.x, u.x), silu_times(a.y, u.y), silu_times(a.z, u.z),
+                                silu_times(a.w, u.w));
+            }
+            const float4 sg = __ldg(reinterpret_cast<const float4*>(signs + k));
+            v[4 * p + 0] = a.x * sg.x;
+            v[4 * p + 1] = a.y * sg.y;
+            v[4 * p + 2] = a.z * sg.z;
+            v[4 * p + 3] = a.w * sg.w;
         }
-        v[p] = a * __ldg(signs + k);
+        // bits 0-1: registers 4p + j, j = 0..3
+#pragma unroll
+        for (int st = 1; st < 4; st <<= 1) {
+#pragma unroll
+            for (int r = 0; r < 32; ++r) {
+                if ((r & st) == 0) {
+                    const float a = v[r], c = v[r + st];
+                    v[r] = a + c;
+                    v[r + st] = a - c;
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int p = 0; p < 32; ++p) {
+            const int k = b * 1024 + 32 * p + lane;
+            const int src = perm ? perm_source(k) : k;
+            float a = __ldg(xm + src);
+            if (SWIGLU) a = silu_times(a, __ldg(xm + K + src));
+            v[p] = a * __ldg(signs + k);
+        }
     }
+    // The lane bits (VEC: element bits 2-6; scalar: bits 0-4): butterflies
+    // across lanes.  The lane with the bit clear holds the low element.
 #pragma unroll
     for (int st = 1; st < 32; st <<= 1) {
 #pragma unroll
-        for (int p = 0; p < 32; ++p) {
-            const float o = __shfl_xor_sync(0xffffffffu, v[p], st);
-            v[p] = (lane & st) ? (o - v[p]) : (v[p] + o);
+        for (int r = 0; r < 32; ++r) {
+            const float o = __shfl_xor_sync(0xffffffffu, v[r], st);
+            v[r] = (lane & st) ? (o - v[r]) : (v[r] + o);
         }
     }
+    // The remaining bits across registers (VEC: register bits 2-4, element
+    // bits 7-9; scalar: register bits 0-4, element bits 5-9).
 #pragma unroll
-    for (int st = 1; st < 32; st <<= 1) {
+    for (int st = VEC ? 4 : 1; st < 32; st <<= 1) {
 #pragma unroll
-        for (int p = 0; p < 32; ++p) {
-            if ((p & st) == 0) {
-                const float a = v[p], c = v[p + st];
-                v[p] = a + c;
-                v[p + st] = a - c;
+        for (int r = 0; r < 32; ++r) {
+            if ((r & st) == 0) {
+                const float a = v[r], c = v[r + st];
+                v[r] = a + c;
+                v[r + st] = a - c;
             }
         }
     }
-    if (!digits) {
-        __nv_bfloat16* out = xt + (size_t)m * K + (size_t)b * 1024;
-#pragma unroll
-        for (int p = 0; p < 32; ++p) out[32 * p + lane] = __float2bfloat16_rn(v[p] * 0.03125f);
-        return;
-    }
-    __nv_bfloat16* out = xt + (size_t)(4 * m) * K + (size_t)b * 1024;
-#pragma unroll
-    for (int p = 0; p < 32; ++p) {
-        const float t = v[p] * 0.03125f;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(t);
-        const float r1 = t - __bfloat162float(hi);  // exact
-        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-        const float r2 = r1 - __bfloat162float(mid);  // exact
-        const int k = 32 * p + lane;
-        out[k] = hi;
-        out[(size_t)K + k] = mid;
-        out[2 * (size_t)K + k] = __float2bfloat16_rn(r2);
-        out[3 * (size_t)K + k] = __float2bfloat16_rn(0.f);
-    }
+    __nv_bfloat16* out = xt + (size_t)(digits ? 4 * m : m) * K + (size_t)b * 1024;
+    if (VEC)
+        store_rotated_vec(v, out, K, digits, lane);
+    else
+        store_rotated(v, out, K, digits, [lane](int r) { return 32 * r + lane; });
 }
 
 }  // namespace
@@ -100,7 +181,15 @@ cudaError_t bitlin_launch_rotate_bf16(const float* x, const float* signs, int M,
     const long long warps = (long long)M * (K / 1024);
     const int threads = 256;
     const long long blocks = (warps * 32 + threads - 1) / threads;
-    bitlin_rotate_bf16<<<(unsigned)blocks, threads, 0, s>>>(x, signs, M, K, perm, digits, swiglu,
-                                                           static_cast<__nv_bfloat16*>(xt));
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(xt);
+    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (reinterpret_cast<uintptr_t>(signs) & 15) == 0;
+    if (vec && swiglu)
+        bitlin_rotate_bf16<true, true><<<(unsigned)blocks, threads, 0, s>>>(x, signs, M, K, perm, digits, out);
+    else if (vec)
+        bitlin_rotate_bf16<true, false><<<(unsigned)blocks, threads, 0, s>>>(x, signs, M, K, perm, digits, out);
+    else if (swiglu)
+        bitlin_rotate_bf16<false, true><<<(unsigned)blocks, threads, 0, s>>>(x, signs, M, K, perm, digits, out);
+    else
+        bitlin_rotate_bf16<false, false><<<(unsigned)blocks, threads, 0, s>>>(x, signs, M, K, perm, digits, out);
     return cudaGetLastError();
 }

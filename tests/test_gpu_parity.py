@@ -108,7 +108,7 @@ def test_gate_up_decode_sweep(hrb, M):
 @pytest.mark.parametrize("name,M", [("attn_qkv", 4), ("attn_gate", 16), ("attn_q", 8), ("attn_kv", 3),
                                     ("attn_output", 5)])
 def test_attention_shapes_small_batch(hrb, name, M):
-    """The attention-side folded shapes at 2 <= M < 64 (exact tensor path), sampled rows."""
+    """The attention-side folded shapes at small M (decode GEMV to M = 4, exact tensor path above), sampled rows."""
     w, bits, scales, signs, x = inputs(name, M)
     y = run(make_layer(hrb, bits, scales, signs, w.perm), x)
     rows = synth.sample_rows(w.seed, w.N, 768)
@@ -286,7 +286,30 @@ def test_forward_host_buffers(hrb, name, M):
     assert max_rel_l2(y.astype(np.float64), ref) <= (DECODE_TOL if M < 64 else PREFILL_TOL)
 
 
-# ------------------------------------------------------------------ exact tensor path (2 <= M < 64)
+# ------------------------------------------------------------------ exact tensor path (5 <= M < 64; any M forced)
+
+@pytest.mark.parametrize("M,perm", [(70, 0), (9, 0), (9, 1)])
+def test_rotation_with_unaligned_activations(hrb, M, perm):
+    """x at an address that is not 16-byte aligned (a view one float into a buffer) takes the
+    rotation's scalar loads: the same y, bit for bit, as from an aligned copy, on the bf16
+    (M = 70) and the exact (M = 9) tensor paths, with and without the permutation."""
+    K, N = 6144, 320
+    seed = 71 + M + perm
+    bits, scales = synth.random_bits(seed, N, K), synth.random_scales(seed, N, K, 0.005, 0.03)
+    signs, x = synth.random_signs(seed, K), synth.random_x(seed, M, K)
+    layer = make_layer(hrb, bits, scales, signs, perm)
+    aligned = torch.from_numpy(x).cuda()
+    buf = torch.empty(M * K + 1, dtype=torch.float32, device="cuda")
+    shifted = buf[1:].view(M, K)
+    shifted.copy_(aligned)
+    assert shifted.data_ptr() % 16 != 0
+    y1, y2 = layer(aligned), layer(shifted)
+    torch.cuda.synchronize()
+    assert layer.get_error() == 0
+    assert torch.equal(y1, y2)
+    ref = oracle.forward(bits, scales, signs, perm, x)
+    assert max_rel_l2(y1.cpu().numpy().astype(np.float64), ref) <= (PREFILL_TOL if M >= 64 else DECODE_TOL)
+
 
 @pytest.mark.parametrize("M,N,K,perm", [(2, 256, 1024, 0), (16, 1000, 2048, 0), (17, 384, 6144, 1),
                                         (40, 300, 3072, 0), (63, 129, 1024, 0), (100, 200, 1024, 0)])
