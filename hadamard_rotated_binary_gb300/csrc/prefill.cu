@@ -162,9 +162,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = bar->tmem_base;
     const uint32_t tmemA = tmem + 2 * BN;  // A stages follow the two accumulator buffers
+    // Programmatic dependent launch: the next kernel may launch once every CTA
+    // of this grid has started.  Only the B loader (xt, written by the
+    // rotation) and the epilogue (y) wait for the previous kernel; the bits,
+    // the scales and the +-1 expansion do not depend on it.
+    ptx::griddep_launch_dependents();
 
     if (warp == kTmaWarp) {
         if (lane == 0) {
+            ptx::griddep_wait();
             // B tiles; stage g % SB is free once the MMAs of group g - SB completed.
             int issued = 0;
             for (int g = 0; g < G; ++g) {
@@ -269,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive(&bar->fullA[sa]);
         }
     } else if (warp < kEpiWarps) {
+        ptx::griddep_wait();
         const int q = warp & 3, half = warp >> 2;
         const int r = 32 * q + lane;
         const int n = n0 + r;
@@ -398,18 +405,20 @@ cudaError_t launch(const PrefillParams& p, const void* tmap, const void* tmap_bi
     }
     const CUtensorMap tb = *static_cast<const CUtensorMap*>(tmap);
     const CUtensorMap tbits = *static_cast<const CUtensorMap*>(tmap_bits);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = splits;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = splits;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(gx, gy, splits);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem_bytes<BN>();
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = splits > 1 ? 1 : 0;
+    cfg.numAttrs = splits > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, bitlin_tc_gemm<BN, EXACT>, tb, tbits, p, stall_test);
 }
 

@@ -143,6 +143,14 @@ __device__ __forceinline__ bool elect_one()
 }
 
 // ---- thread-block clusters (distributed shared memory) ----------------------
+// Programmatic dependent launch: wait until the grids this one depends on have
+// completed and their memory is visible; let the next grid in the stream launch.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");

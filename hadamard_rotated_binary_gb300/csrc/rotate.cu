@@ -97,6 +97,11 @@ __global__ void __launch_bounds__(256) bitlin_rotate_bf16(const float* __restric
                                                           const float* __restrict__ signs, int M, int K,
                                                           int perm, int digits, __nv_bfloat16* __restrict__ xt)
 {
+    // Programmatic dependent launch: the GEMM that reads xt may launch (and set
+    // up) while this grid runs; x may come from the previous kernel, so wait for
+    // it before reading.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int B = K / 1024;
@@ -183,13 +188,17 @@ cudaError_t bitlin_launch_rotate_bf16(const float* x, const float* signs, int M,
     const long long blocks = (warps * 32 + threads - 1) / threads;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(xt);
     const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (reinterpret_cast<uintptr_t>(signs) & 15) == 0;
-    if (vec && swiglu)
-        bitlin_rotate_bf16<true, true><<<(unsigned)blocks, threads, 0, s>>>(x, signs, M, K, perm, digits, out);
-    else if (vec)
-        bitlin_rotate_bf16<true, false><<<(unsigned)blocks, threads, 0, s>>>(x, signs, M, K, perm, digits, out);
-    else if (swiglu)
-        bitlin_rotate_bf16<false, true><<<(unsigned)blocks, threads, 0, s>>>(x, signs, M, K, perm, digits, out);
-    else
-        bitlin_rotate_bf16<false, false><<<(unsigned)blocks, threads, 0, s>>>(x, signs, M, K, perm, digits, out);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (vec && swiglu) return cudaLaunchKernelEx(&cfg, bitlin_rotate_bf16<true, true>, x, signs, M, K, perm, digits, out);
+    if (vec) return cudaLaunchKernelEx(&cfg, bitlin_rotate_bf16<true, false>, x, signs, M, K, perm, digits, out);
+    if (swiglu) return cudaLaunchKernelEx(&cfg, bitlin_rotate_bf16<false, true>, x, signs, M, K, perm, digits, out);
+    return cudaLaunchKernelEx(&cfg, bitlin_rotate_bf16<false, false>, x, signs, M, K, perm, digits, out);
 }
