@@ -161,8 +161,8 @@ def max_over_ranks(v: float, pg, device) -> float:
 
 
 def uses_decode(w: synth.Workload, path: str = "auto") -> bool:
-    """Whether the library runs the decode GEMV for this call (its own choice: M <= 4)."""
-    return path == "decode" or (path == "auto" and w.M <= 4)
+    """Whether the library runs the decode GEMV for this call (its own choice: M <= 6)."""
+    return path == "decode" or (path == "auto" and w.M <= 6)
 
 
 def path_of(w: synth.Workload, path: str = "auto") -> str:

@@ -26,10 +26,11 @@ constexpr int kLutBytes = 65536;      // 64 octet tables x 256 entries x f32
 constexpr int kPrefillRows = 128;     // weight rows per CTA (UMMA M)
 constexpr int kPrefillTokens = 128;   // tokens per CTA (UMMA N)
 constexpr int kPrefillMinM = 64;      // auto path: bf16 tensor path from this M
-// Auto path: the decode GEMV up to this M (tokens one after the other, each
-// with its own tables; measured faster than the exact tensor path up to 2-4
-// tokens, e.g. gate_up 5120 x 34816 at M = 4: 33 us against 55 us).
-constexpr int kDecodeMaxM = 4;
+// Auto path: the decode GEMV up to this M (tokens two at a time, each pair
+// with its own tables).  Measured against the exact tensor path: gate_up
+// 5120 x 34816 at M = 6: 34.1 us against 38.3 us, at M = 8: 44.2 against 38.5;
+// ffn_down 17408 x 5120 at M = 6: 23.7 against 24.7, at M = 8: 29.1 against 24.8.
+constexpr int kDecodeMaxM = 6;
 
 // Device-side error word values (bitlin_t::dev_error).
 constexpr int kDevErrTimeout = 1;

@@ -1,4 +1,4 @@
-// Decode GEMV (the library's choice for M <= 4; any M when forced): activation
+// Decode GEMV (the library's choice for M <= 6; any M when forced): activation
 // rotation fused into the prologue, then the one-bit product through
 // shared-memory signed-sum tables.
 //

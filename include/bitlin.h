@@ -25,9 +25,9 @@
  * sum then one multiply by the scale; station on the embedding row: bit k is
  * bit k&31 of word k>>5, scale index k>>7, IEEE binary16 scales).
  *
- * Paths: 1 <= M <= 4 runs the decode GEMV (f32 throughout; expected max
+ * Paths: 1 <= M <= 6 runs the decode GEMV (f32 throughout; expected max
  * relative L2 error per token row <= 1e-5 against an exact evaluation).
- * 5 <= M < 64 runs the tensor-core path with xt split exactly into three bf16
+ * 7 <= M < 64 runs the tensor-core path with xt split exactly into three bf16
  * digits, so the +-1 x digit products and f32 accumulation give f32-level
  * results (<= 1e-5).
  * M >= 64 runs the tensor-core path with xt rounded to bf16 (<= 1e-2).  In
@@ -70,7 +70,7 @@ typedef enum {
  * (Pulse "ARCHITECTURE-SPEC", ssm_out permutation paragraph.) */
 #define BITLIN_PERM_SSM_TILED_TO_GROUPED 1
 
-#define BITLIN_PATH_AUTO 0     /* M <= 4 -> decode GEMV, 5 <= M < 64 -> exact tensor path, M >= 64 -> prefill */
+#define BITLIN_PATH_AUTO 0     /* M <= 6 -> decode GEMV, 7 <= M < 64 -> exact tensor path, M >= 64 -> prefill */
 #define BITLIN_PATH_DECODE 1   /* force the f32 decode GEMV (shared-memory tables) for every M */
 #define BITLIN_PATH_PREFILL 2  /* force the tcgen05 path with bf16 activations for every M */
 #define BITLIN_PATH_TC_EXACT 3 /* force the tcgen05 path with activations split into three bf16

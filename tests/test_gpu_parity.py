@@ -108,7 +108,7 @@ def test_gate_up_decode_sweep(hrb, M):
 @pytest.mark.parametrize("name,M", [("attn_qkv", 4), ("attn_gate", 16), ("attn_q", 8), ("attn_kv", 3),
                                     ("attn_output", 5)])
 def test_attention_shapes_small_batch(hrb, name, M):
-    """The attention-side folded shapes at small M (decode GEMV to M = 4, exact tensor path above), sampled rows."""
+    """The attention-side folded shapes at small M (decode GEMV to M = 6, exact tensor path above), sampled rows."""
     w, bits, scales, signs, x = inputs(name, M)
     y = run(make_layer(hrb, bits, scales, signs, w.perm), x)
     rows = synth.sample_rows(w.seed, w.N, 768)
@@ -286,7 +286,7 @@ def test_forward_host_buffers(hrb, name, M):
     assert max_rel_l2(y.astype(np.float64), ref) <= (DECODE_TOL if M < 64 else PREFILL_TOL)
 
 
-# ------------------------------------------------------------------ exact tensor path (5 <= M < 64; any M forced)
+# ------------------------------------------------------------------ exact tensor path (7 <= M < 64; any M forced)
 
 @pytest.mark.parametrize("M,perm", [(70, 0), (9, 0), (9, 1)])
 def test_rotation_with_unaligned_activations(hrb, M, perm):
@@ -330,13 +330,13 @@ def test_tc_exact_path_every_tile_width(hrb, M, N, K, perm):
 
 
 def test_auto_path_choice(hrb):
-    """M <= 4 -> table GEMV, 5..63 -> exact tensor path, >= 64 -> bf16 tensor path; all in tolerance."""
+    """M <= 6 -> table GEMV, 7..63 -> exact tensor path, >= 64 -> bf16 tensor path; all in tolerance."""
     w, bits, scales, signs, x = inputs("ffn_gate", 70)
     layer = make_layer(hrb, bits, scales, signs, 0)
     rows = synth.sample_rows(w.seed, w.N, 256)
     ref = oracle.forward(bits, scales, signs, 0, x, rows)
-    for m, tol in ((1, DECODE_TOL), (2, DECODE_TOL), (4, DECODE_TOL), (5, DECODE_TOL), (63, DECODE_TOL),
-                   (64, PREFILL_TOL), (70, PREFILL_TOL)):
+    for m, tol in ((1, DECODE_TOL), (2, DECODE_TOL), (5, DECODE_TOL), (6, DECODE_TOL), (7, DECODE_TOL),
+                   (63, DECODE_TOL), (64, PREFILL_TOL), (70, PREFILL_TOL)):
         y = run(layer, np.ascontiguousarray(x[:m]))
         assert max_rel_l2(y[:, rows], ref[:m]) <= tol, m
 
@@ -347,7 +347,7 @@ def test_plan_reports_path_and_kernels(hrb):
     paths; a forced path is reported as forced."""
     gate = make_layer(hrb, *inputs("ffn_gate", 1)[1:4], 0)
     down = make_layer(hrb, *inputs("ffn_down", 1)[1:4], 0)
-    assert [gate.plan(m) for m in (1, 2, 4, 5, 63, 64)] == [(1, 1), (1, 1), (1, 1), (3, 2), (3, 2), (2, 2)]
+    assert [gate.plan(m) for m in (1, 2, 6, 7, 63, 64)] == [(1, 1), (1, 1), (1, 1), (3, 2), (3, 2), (2, 2)]
     assert down.plan(1) == (1, 2)
     gate.set_path(1)
     assert gate.plan(200) == (1, 2)  # 200 tokens' partials do not fit shared memory: scratch + sum
