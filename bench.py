@@ -160,34 +160,25 @@ def max_over_ranks(v: float, pg, device) -> float:
     return float(t.item())
 
 
-def uses_decode(w: synth.Workload, path: str = "auto") -> bool:
-    """Whether the library runs the decode GEMV for this call (its own choice: M <= 6)."""
-    return path == "decode" or (path == "auto" and w.M <= 6)
-
-
-def path_of(w: synth.Workload, path: str = "auto") -> str:
-    """Kernel that does the bulk of one call: the decode GEMV or the tcgen05 GEMM."""
-    return "bitlin_decode_gemv" if uses_decode(w, path) else "bitlin_tc_gemm"
-
-
-def roofline(w: synth.Workload, s_per_step: float, peaks: dict, peak_kind: str, path: str = "auto",
-             kernels: int = 1) -> dict:
-    """Roofline of the dominant kernel.  Decode: HBM-bound, algorithmic bytes per call over the
-    step time (one GEMV per step; with kernels = 2 the step also holds the small split-K sum,
-    which the GEMV overlaps through programmatic dependent launch, so the fraction is a lower
-    bound).  Tensor paths: the tcgen05 GEMM, 2*M*N*K bf16 MMA flops per launch (the exact path
-    multiplies three bf16 digit columns per token, 3x that) over the step time, which also holds
-    the small rotation kernel, so the fraction is a lower bound; peak = the measured burst bf16
-    GEMM rate (the timed loop lasts milliseconds)."""
-    kernel = path_of(w, path)
-    if uses_decode(w, path) and kernels == 2:
-        kernel = "bitlin_decode_gemv + bitlin_decode_reduce"
-    if uses_decode(w, path):
+def roofline(w: synth.Workload, s_per_step: float, peaks: dict, peak_kind: str, path: int,
+             kernels: int) -> dict:
+    """Roofline of the dominant kernel of a call on `path` (the library's BITLIN_PATH_*, from
+    bitlin_plan: 1 decode, 2 bf16 tensor path, 3 exact tensor path) launching `kernels` kernels.
+    Decode: HBM-bound, algorithmic bytes per call over the step time (one GEMV per step; with
+    kernels = 2 the step also holds the small split-K sum, which the GEMV overlaps through
+    programmatic dependent launch, so the fraction is a lower bound).  Tensor paths: the tcgen05
+    GEMM, 2*M*N*K bf16 MMA flops per launch (the exact path multiplies three bf16 digit columns per
+    token, 3x that) over the step time, which also holds the small rotation kernel, so the
+    fraction is a lower bound; peak = the measured burst bf16 GEMM rate (the timed loop lasts
+    milliseconds)."""
+    if path == 1:
+        kernel = "bitlin_decode_gemv" + (" + bitlin_decode_reduce" if kernels == 2 else "")
         achieved = w.algorithmic_bytes() / s_per_step / 1e9
         return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_kind": peak_kind, "kernel": kernel,
                 "bytes_per_launch": w.algorithmic_bytes(), "traffic": traffic_record(kernel, w.name)}
-    digits = 3 if (path == "exact" or (path == "auto" and w.M < 64)) else 1
+    kernel = "bitlin_tc_gemm"
+    digits = 3 if path == 3 else 1
     flops = 2.0 * w.M * digits * w.N * w.K
     achieved = flops / s_per_step / 1e12
     return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -637,7 +628,7 @@ def main():
 
     peaks, peak_kind = measured_peaks()
     s_per_step = ms / 1e3 / args.steps
-    kernels = layers[0].plan(w.M)[1]
+    path, kernels = layers[0].plan(w.M)
     tokens_per_s = ws * w.M / s_per_step
     algo_bytes = w.algorithmic_bytes()
     achieved = algo_bytes / s_per_step / 1e9
@@ -652,15 +643,17 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": "f32" if path == hrb.PATH_DECODE else "bf16",
         "data": "synthetic (seeded SplitMix64: Bernoulli(0.5) bits, U[0.005,0.03] fp16 scales, +-1 signs, N(0,1) x)",
         "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "perm": w.perm, "path": args.path,
+                   "kernel_path": {1: "decode GEMV (f32)", 2: "tcgen05, bf16 activations",
+                                   3: "tcgen05, three exact bf16 digits, f32 accumulation"}[path],
                    "weight_copies": R, "weight_set_bytes": R * wbytes,
                    "l2": f"inputs larger than L2: {R} distinct weight copies ({R * wbytes / 1e6:.0f} MB) cycled",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "weight_gbs": w.weight_bytes() / s_per_step / 1e9,
         "hbm_frac_of_8tbs": achieved / 8000.0,
-        "roofline": roofline(w, s_per_step, peaks, peak_kind, args.path, kernels),
+        "roofline": roofline(w, s_per_step, peaks, peak_kind, path, kernels),
         "gpu_launches": args.steps * kernels,  # the library's own count per call (bitlin_plan)
         "clocks": clocks,
         "e2e": {"value": ws * w.M * e2e_steps / e2e_s, "unit": UNIT,
