@@ -48,8 +48,13 @@
 //  * Programmatic dependent launch: the kernel lets its successor launch after
 //    its table build and itself waits (griddepcontrol.wait) only before it
 //    reads x or writes any output.  Before the wait it issues what does not
-//    depend on the previous kernel: an L2 prefetch of its whole weight share,
-//    the first ring of tiles, the signs, and an L2 hint for the lines of x.
+//    depend on the previous kernel: the first ring of tiles, the signs, an L2
+//    hint for the lines of x and, on the scratch split-K path, an L2 prefetch
+//    of the first part of its weight share.
+//  * Every instruction before the lookups is on a call's critical path (the
+//    CTAs that start last, on SMs whose previous CTA ended last, set the
+//    call's time), so the tile-range split and the partial-sum placement use
+//    32-bit arithmetic and no runtime division.
 #include <cuda_fp16.h>
 
 #include "bitlin_internal.cuh"
@@ -389,10 +394,9 @@ __device__ __forceinline__ void cluster_finish(const DecodeParams& p, int ta, in
     ptx::cluster_sync();
     const int ntile = tb - ta, S = p.S, LT = cluster_slots(ntile, S);
     const int mine = ntile > rank ? (ntile - rank + S - 1) / S : 0;  // tiles rank, rank + S, ...
-    const int rows = p.M * mine * kTileRows;
-    for (int i = (int)threadIdx.x; i < rows; i += kDecodeThreads) {
-        const int m = i / (mine * kTileRows), rem = i - m * mine * kTileRows;
-        const int slot = rem / kTileRows, lane = rem - slot * kTileRows;
+    for (int m = 0; m < p.M; ++m)
+    for (int i = (int)threadIdx.x; i < mine * kTileRows; i += kDecodeThreads) {
+        const int slot = i >> 5, lane = i & 31;
         const float* src = pbuf + (((size_t)m * S) * LT + slot) * kTileRows + lane;
         float sum = 0.f;
         for (int s = 0; s < S; ++s) sum += src[(size_t)s * LT * kTileRows];
@@ -421,16 +425,19 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
     // otherwise (more slices than CTAs) the units are split evenly.
     int u0, u1;
     int rank = 0;  // cluster mode: this CTA's slice = its rank in the cluster
+    // The T tiles of a slice are split over ctas_per_slice = ncl ranges, the
+    // first split_r of them one tile longer: range c starts at
+    // c * split_q + min(c, split_r).  No division in the cluster case.
     if (p.cluster) {
-        // Cluster c (consecutive blocks) covers tiles [T*c/ncl, T*(c+1)/ncl) of every slice.
-        const int ncl = gridDim.x / p.S, c = blockIdx.x / p.S;
-        rank = blockIdx.x - c * p.S;
-        u0 = rank * p.T + (int)((long long)p.T * c / ncl);
-        u1 = rank * p.T + (int)((long long)p.T * (c + 1) / ncl);
+        // Cluster c (S consecutive blocks, one per slice) covers range c of every slice.
+        const int c = (int)__umulhi(blockIdx.x, p.s_mul);  // blockIdx.x / S
+        rank = (int)blockIdx.x - c * p.S;
+        u0 = rank * p.T + c * p.split_q + min(c, p.split_r);
+        u1 = u0 + p.split_q + (c < p.split_r ? 1 : 0);
     } else if (p.ctas_per_slice > 0) {
-        const int s = blockIdx.x / p.ctas_per_slice, c = blockIdx.x - s * p.ctas_per_slice;
-        u0 = s * p.T + (int)((long long)p.T * c / p.ctas_per_slice);
-        u1 = s * p.T + (int)((long long)p.T * (c + 1) / p.ctas_per_slice);
+        const int s = (int)blockIdx.x / p.ctas_per_slice, c = (int)blockIdx.x - s * p.ctas_per_slice;
+        u0 = s * p.T + c * p.split_q + min(c, p.split_r);
+        u1 = u0 + p.split_q + (c < p.split_r ? 1 : 0);
     } else {
         const long long U = (long long)p.S * p.T;
         u0 = (int)(U * blockIdx.x / gridDim.x);
@@ -441,13 +448,14 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
     const uint32_t base_off = (uint32_t)(4 * (lane & 15) + 64 * (lane >> 4)) |
                               ((uint32_t)(4 * (lane & 15) + 64 * (1 - (lane >> 4))) << 8);
 
-    // The weights do not depend on the previous kernel: start streaming this
-    // CTA's whole share (one contiguous range of bits and one of scales) from
-    // HBM into L2 before waiting for it.
-    // At most the first kPrefetchUnits units: for matrices larger than L2 (the
-    // 179 MB vocabulary matrix) a prefetch of everything would evict itself
-    // before use; the register ring streams the rest.
-    {
+    // The weights do not depend on the previous kernel.  On the scratch
+    // split-K path, start streaming the first kPrefetchUnits units of this
+    // CTA's share (one contiguous range of bits and one of scales) from HBM
+    // into L2 before waiting for it (a prefetch of everything would evict
+    // itself on matrices larger than L2).  The cluster path issues only its
+    // register ring: there the extra requests measured slower (ffn_gate 6.39
+    // against 6.74 us per call without them, the LM head 45.9 against 46.5).
+    if (!p.cluster) {
         const int pu = min(u1 - u0, kPrefetchUnits);
         prefetch_l2(p.bits + (size_t)u0 * 128, (size_t)pu * 2048, threadIdx.x);
         prefetch_l2(p.scales + (size_t)u0 * 32, (size_t)pu * 256, (threadIdx.x + 128) % kDecodeThreads);
@@ -527,8 +535,11 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
             auto put = [&](int mm, int t, float v) {
                 if (p.cluster) {
                     const int lt = t - ta;
-                    const uint32_t off = (uint32_t)((((mm * p.S) + rank) * LT + lt / p.S) * kTileRows + lane);
-                    ptx::st_cluster(ptx::cluster_map(pbase + 4u * off, lt % p.S), v);
+                    // lt / S as umulhi(lt, ceil(2^32 / S)): exact for S in [2, 16], lt < 2^17
+                    // (the partials of a cluster fit 96 KB, so lt < 768).
+                    const int q = (int)__umulhi((unsigned)lt, p.s_mul), r = lt - q * p.S;
+                    const uint32_t off = (uint32_t)((((mm * p.S) + rank) * LT + q) * kTileRows + lane);
+                    ptx::st_cluster(ptx::cluster_map(pbase + 4u * off, r), v);
                 } else {
                     p.partials[((size_t)s * p.M + mm) * npad + (size_t)t * kTileRows + lane] = v;
                 }
@@ -673,6 +684,7 @@ DecodeShape decode_shape(const DecodeParams& p, int num_sms, DecodeParams& q)
     q = p;
     DecodeShape d{0, p.M >= 2 ? kPbufOff2 : kDecodeSmem, 0};  // two tables from M = 2
     q.cluster = 0;
+    q.s_mul = 0xFFFFFFFFu / (unsigned)p.S + 1u;  // ceil(2^32 / S); S = K / 512 >= 2
     // Split-K across a cluster when the slices fit one (S <= 16) and the
     // partial sums fit shared memory; else through the global scratch.
     if (p.allow_cluster && p.S <= kMaxClusterSlices) {
@@ -700,6 +712,10 @@ DecodeShape decode_shape(const DecodeParams& p, int num_sms, DecodeParams& q)
             q.ctas_per_slice = 0;
             d.grid = (int)(U < num_sms ? U : num_sms);
         }
+    }
+    if (q.ctas_per_slice > 0) {
+        q.split_q = p.T / q.ctas_per_slice;
+        q.split_r = p.T - q.split_q * q.ctas_per_slice;
     }
     return d;
 }
