@@ -427,19 +427,32 @@ constexpr int kDecodeRegs = BITLIN_DECODE_REGS;
 // and arithmetic as the global-scratch path) from its own shared memory, and
 // writes y.  Nothing reads another CTA's shared memory after the barrier, so
 // no second barrier is needed before the CTAs exit.
-__device__ __forceinline__ int cluster_slots(int ntile, int S) { return (ntile + S - 1) / S; }
+// v / S as umulhi(v, ceil(2^32 / S)): exact for S in [2, 16] and v < 2^17 (the
+// partial sums of a cluster fit 96 KB, so its tile count is below 768).
+__device__ __forceinline__ int div_s(const DecodeParams& p, int v) { return (int)__umulhi((unsigned)v, p.s_mul); }
+__device__ __forceinline__ int cluster_slots(const DecodeParams& p, int ntile) { return div_s(p, ntile + p.S - 1); }
 
 __device__ __forceinline__ void cluster_finish(const DecodeParams& p, int ta, int tb, int rank, const float* pbuf)
 {
     ptx::cluster_sync();
-    const int ntile = tb - ta, S = p.S, LT = cluster_slots(ntile, S);
-    const int mine = ntile > rank ? (ntile - rank + S - 1) / S : 0;  // tiles rank, rank + S, ...
+    const int ntile = tb - ta, S = p.S, LT = cluster_slots(p, ntile);
+    const int mine = ntile > rank ? div_s(p, ntile - rank + S - 1) : 0;  // tiles rank, rank + S, ...
+    const int stride = LT * kTileRows;
     for (int m = 0; m < p.M; ++m)
     for (int i = (int)threadIdx.x; i < mine * kTileRows; i += kDecodeThreads) {
         const int slot = i >> 5, lane = i & 31;
-        const float* src = pbuf + (((size_t)m * S) * LT + slot) * kTileRows + lane;
+        const float* src = pbuf + (m * S * LT + slot) * kTileRows + lane;
+        // All S loads in flight at once, then the sum in slice order.
+        float v[kMaxClusterSlices];
+#pragma unroll
+        for (int s = 0; s < kMaxClusterSlices; ++s) {
+            v[s] = 0.f;
+            if (s < S) v[s] = src[s * stride];
+        }
         float sum = 0.f;
-        for (int s = 0; s < S; ++s) sum += src[(size_t)s * LT * kTileRows];
+#pragma unroll
+        for (int s = 0; s < kMaxClusterSlices; ++s)
+            if (s < S) sum += v[s];
         const int n = (ta + slot * S + rank) * kTileRows + lane;
         if (n < p.N) p.y[(size_t)m * p.N + n] = sum;
     }
@@ -580,7 +593,7 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
             // Partial sums.  Scratch path: token mm, tile t, lane ->
             // partials[s][mm][t * 32 + lane].  Cluster path: into the owner's shared
             // memory (see cluster_finish).
-            const int LT = cluster_slots(tb - ta, p.S);
+            const int LT = p.cluster ? cluster_slots(p, tb - ta) : 0;
             const uint32_t pbase = static_cast<uint32_t>(__cvta_generic_to_shared(pbuf));
             auto put = [&](int mm, int t, float v) {
                 if (p.cluster) {
