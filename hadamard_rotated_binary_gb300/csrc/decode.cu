@@ -111,9 +111,16 @@ __device__ __forceinline__ void load_tile(const DecodeParams& p, int s, int t, i
 {
     const size_t unit = (size_t)s * p.T + t;
     const uint4* src = p.bits + unit * 4 * 32 + lane;
+    // Each weight byte is read once: no L1 allocation (the vocabulary matrix
+    // measured 44.6 against 45.4 us per call).
 #pragma unroll
-    for (int q = 0; q < 4; ++q) b[q] = __ldg(src + q * 32);
-    sc = __ldg(p.scales + unit * 32 + lane);
+    for (int q = 0; q < 4; ++q)
+        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(b[q].x), "=r"(b[q].y), "=r"(b[q].z), "=r"(b[q].w)
+                     : "l"(src + q * 32));
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(sc.x), "=r"(sc.y)
+                 : "l"(p.scales + unit * 32 + lane));
 }
 
 // Source column of grouped position k under the ssm_out permutation
