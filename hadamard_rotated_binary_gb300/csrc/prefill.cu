@@ -280,9 +280,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = 32 * q + lane;
         const int n = n0 + r;
         const bool valid = n < p.N;
-        float acc[kAcc];
+        // Accumulators in pairs: the exact mode sums two outputs' digit columns
+        // and scales them with packed f32x2 adds and FMAs (__fadd2_rn,
+        // __ffma2_rn; gate_up at M = 16: 38.8 -> 38.3 us).  The bf16 mode keeps
+        // scalar FMAs: its packed pairs exceeded the 128-register budget.
+        static_assert(kAcc % 2 == 0, "accumulators come in pairs");
+        float2 acc2[kAcc / 2];
 #pragma unroll
-        for (int j = 0; j < kAcc; ++j) acc[j] = 0.f;
+        for (int j = 0; j < kAcc / 2; ++j) acc2[j] = make_float2(0.f, 0.f);
         const uint16_t* srow = p.scales + (size_t)(valid ? n : 0) * Gall + gbase;
         // The row's scales, requested kSRing groups ahead.
         constexpr int kSRing = 4;
@@ -315,13 +320,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tc_fence_before();
                         ptx::mbar_arrive(&bar->tempty[buf]);
                     }
+                    const float2 s2 = make_float2(s, s);
                     if (EXACT) {
 #pragma unroll
-                        for (int t = 0; t < 8; ++t)
-                            acc[8 * c + t] = fmaf(s, (v[4 * t] + v[4 * t + 1]) + v[4 * t + 2], acc[8 * c + t]);
+                        for (int t = 0; t < 8; t += 2) {
+                            const float2 d = __fadd2_rn(__fadd2_rn(make_float2(v[4 * t], v[4 * t + 4]),
+                                                                   make_float2(v[4 * t + 1], v[4 * t + 5])),
+                                                        make_float2(v[4 * t + 2], v[4 * t + 6]));
+                            acc2[(8 * c + t) / 2] = __ffma2_rn(s2, d, acc2[(8 * c + t) / 2]);
+                        }
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(s, v[j], acc[32 * c + j]);
+                        for (int j = 0; j < 32; j += 2) {
+                            acc2[(32 * c + j) / 2].x = fmaf(s, v[j], acc2[(32 * c + j) / 2].x);
+                            acc2[(32 * c + j) / 2].y = fmaf(s, v[j + 1], acc2[(32 * c + j) / 2].y);
+                        }
                     }
                 }
             }
@@ -332,12 +345,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // column c = half * kAcc + j, row r: pbuf[c * 128 + r].
             float* pbuf = reinterpret_cast<float*>(tileB);
 #pragma unroll
-            for (int j = 0; j < kAcc; ++j) pbuf[(half * kAcc + j) * kPrefillRows + r] = acc[j];
+            for (int j = 0; j < kAcc; ++j) pbuf[(half * kAcc + j) * kPrefillRows + r] = (j & 1) ? acc2[j / 2].y : acc2[j / 2].x;
         } else if (ok && valid) {
 #pragma unroll
             for (int j = 0; j < kAcc; ++j) {
                 const int m = EXACT ? (b0 + half * kHalf) / 4 + j : b0 + half * kHalf + j;
-                if (m < p.M) p.y[(size_t)m * p.N + n] = acc[j];
+                if (m < p.M) p.y[(size_t)m * p.N + n] = (j & 1) ? acc2[j / 2].y : acc2[j / 2].x;
             }
         }
     }
