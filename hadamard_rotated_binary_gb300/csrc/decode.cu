@@ -494,6 +494,7 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
     // ctas_per_slice > 0 every CTA stays inside one slice (one table build);
     // otherwise (more slices than CTAs) the units are split evenly.
     int u0, u1;
+    int s0;        // the slice of the CTA's first segment
     int rank = 0;  // cluster mode: this CTA's slice = its rank in the cluster
     // The T tiles of a slice are split over ctas_per_slice = ncl ranges, the
     // first split_r of them one tile longer: range c starts at
@@ -502,16 +503,19 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
         // Cluster c (S consecutive blocks, one per slice) covers range c of every slice.
         const int c = (int)__umulhi(blockIdx.x, p.s_mul);  // blockIdx.x / S
         rank = (int)blockIdx.x - c * p.S;
+        s0 = rank;
         u0 = rank * p.T + c * p.split_q + min(c, p.split_r);
         u1 = u0 + p.split_q + (c < p.split_r ? 1 : 0);
     } else if (p.ctas_per_slice > 0) {
         const int s = (int)blockIdx.x / p.ctas_per_slice, c = (int)blockIdx.x - s * p.ctas_per_slice;
+        s0 = s;
         u0 = s * p.T + c * p.split_q + min(c, p.split_r);
         u1 = u0 + p.split_q + (c < p.split_r ? 1 : 0);
     } else {
         const long long U = (long long)p.S * p.T;
         u0 = (int)(U * blockIdx.x / gridDim.x);
         u1 = (int)(U * (blockIdx.x + 1) / gridDim.x);
+        s0 = u0 / p.T;
     }
     const size_t npad = (size_t)p.T * kTileRows;
     // Per-lane part of every table offset: byte 0 for even bytes, byte 1 for odd.
@@ -537,7 +541,7 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
     uint2 rs[RING];
     float xv[4 * kRowsPerWarp];
     {
-        const int s = u0 / p.T, ta = u0 - s * p.T, tb = min(p.T, ta + (u1 - u0));
+        const int s = s0, ta = u0 - s * p.T, tb = min(p.T, ta + (u1 - u0));
 #pragma unroll
         for (int d = 0; d < RING; ++d) {
             const int t = ta + warp + kDecodeWarps * d;
@@ -553,7 +557,7 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
     bool preloaded = true;  // the ring and the signs hold the first (segment, token)
 
     for (int u = u0; u < u1;) {
-        const int s = u / p.T;
+        const int s = u == u0 ? s0 : u / p.T;  // no division before the first segment's loads
         const int ta = u - s * p.T;
         const int tb = min(p.T, ta + (u1 - u));
         u += tb - ta;
@@ -562,7 +566,7 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
         // loaded serves both tokens' lookups.
         for (int m = 0; m < p.M; m += TWO ? 2 : 1) {
             const bool two = TWO && m + 1 < p.M;
-            __syncthreads();  // the previous tables are no longer read
+            if (!preloaded) __syncthreads();  // the previous tables and buffers are no longer read
             if (!preloaded) {
                 slice_load_signs(p, s, warp, lane, xv);
 #pragma unroll
