@@ -106,21 +106,30 @@ __device__ __forceinline__ float lut_at(const unsigned char* lut, uint32_t off)
 // Padded index of slice position i (one spare float every 32).
 __device__ __forceinline__ int xpad(int i) { return i + (i >> 5); }
 
+// NA: loads that allocate nothing in L1 (each weight byte is read once).
+// Measured per call: the one-token LM head 44.5 against 45.3 us with them; the
+// two-token instance on the scratch path slower with them (ffn_down at M = 4:
+// 18.8 against 18.1 us), so it keeps the plain read-only loads.
+template <bool NA>
 __device__ __forceinline__ void load_tile(const DecodeParams& p, int s, int t, int lane, uint4 (&b)[4],
                                           uint2& sc)
 {
     const size_t unit = (size_t)s * p.T + t;
     const uint4* src = p.bits + unit * 4 * 32 + lane;
-    // Each weight byte is read once: no L1 allocation (the vocabulary matrix
-    // measured 44.6 against 45.4 us per call).
+    if (NA) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(b[q].x), "=r"(b[q].y), "=r"(b[q].z), "=r"(b[q].w)
-                     : "l"(src + q * 32));
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
-                 : "=r"(sc.x), "=r"(sc.y)
-                 : "l"(p.scales + unit * 32 + lane));
+        for (int q = 0; q < 4; ++q)
+            asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(b[q].x), "=r"(b[q].y), "=r"(b[q].z), "=r"(b[q].w)
+                         : "l"(src + q * 32));
+        asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                     : "=r"(sc.x), "=r"(sc.y)
+                     : "l"(p.scales + unit * 32 + lane));
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) b[q] = __ldg(src + q * 32);
+        sc = __ldg(p.scales + unit * 32 + lane);
+    }
 }
 
 // Source column of grouped position k under the ssm_out permutation
@@ -160,6 +169,35 @@ __device__ __forceinline__ const float* x_source(const DecodeParams& p, int m, i
 }
 
 __device__ __forceinline__ float swiglu(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+// The addresses slice_load_x reads (they do not depend on the previous
+// kernel, so they can be formed before the wait for it).
+__device__ __forceinline__ void slice_x_ptrs(const DecodeParams& p, int m, int s, int warp, int lane,
+                                             const float* (&a)[2 * kRowsPerWarp])
+{
+    const int b = s >> 1;
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        const int k0 = b * 1024 + 32 * (warp + kDecodeWarps * r) + lane;
+        a[2 * r + 0] = x_source(p, m, k0);
+        a[2 * r + 1] = x_source(p, m, k0 + 512);
+    }
+}
+
+__device__ __forceinline__ void slice_load_x_at(const DecodeParams& p, const float* const (&a)[2 * kRowsPerWarp],
+                                                float (&v)[4 * kRowsPerWarp])
+{
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        if (p.swiglu) {
+            v[4 * r + 0] = swiglu(__ldg(a[2 * r]), __ldg(a[2 * r] + p.K));
+            v[4 * r + 2] = swiglu(__ldg(a[2 * r + 1]), __ldg(a[2 * r + 1] + p.K));
+        } else {
+            v[4 * r + 0] = __ldg(a[2 * r]);
+            v[4 * r + 2] = __ldg(a[2 * r + 1]);
+        }
+    }
+}
 
 __device__ __forceinline__ void slice_load_x(const DecodeParams& p, int m, int s, int warp, int lane,
                                              float (&v)[4 * kRowsPerWarp])
@@ -540,16 +578,20 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
     uint4 rb[RING][4];
     uint2 rs[RING];
     float xv[4 * kRowsPerWarp];
+    // One token: the first segment's x addressed before the wait (ffn_gate 5.69
+    // -> 5.63 us; the two-token instance measured slower with it).
+    const float* xptr[2 * kRowsPerWarp];
     {
         const int s = s0, ta = u0 - s * p.T, tb = min(p.T, ta + (u1 - u0));
 #pragma unroll
         for (int d = 0; d < RING; ++d) {
             const int t = ta + warp + kDecodeWarps * d;
-            if (u0 < u1 && t < tb) load_tile(p, s, t, lane, rb[d], rs[d]);
+            if (u0 < u1 && t < tb) load_tile<!TWO>(p, s, t, lane, rb[d], rs[d]);
         }
         if (u0 < u1) {
             slice_load_signs(p, s, warp, lane, xv);
             slice_prefetch_x(p, 0, s, warp, lane);
+            if (!TWO) slice_x_ptrs(p, 0, s, warp, lane, xptr);
         }
     }
     pdl_wait();
@@ -566,20 +608,22 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
         // loaded serves both tokens' lookups.
         for (int m = 0; m < p.M; m += TWO ? 2 : 1) {
             const bool two = TWO && m + 1 < p.M;
+            const bool first = preloaded;
             if (!preloaded) __syncthreads();  // the previous tables and buffers are no longer read
             if (!preloaded) {
                 slice_load_signs(p, s, warp, lane, xv);
 #pragma unroll
                 for (int d = 0; d < RING; ++d) {
                     const int t = ta + warp + kDecodeWarps * d;
-                    if (t < tb) load_tile(p, s, t, lane, rb[d], rs[d]);
+                    if (t < tb) load_tile<!TWO>(p, s, t, lane, rb[d], rs[d]);
                 }
             }
             preloaded = false;
             float xv2[4 * kRowsPerWarp];
 #pragma unroll
             for (int i = 0; i < 4 * kRowsPerWarp; ++i) xv2[i] = xv[i];  // the signs
-            slice_load_x(p, m, s, warp, lane, xv);
+            if (!TWO && first) slice_load_x_at(p, xptr, xv);
+            else slice_load_x(p, m, s, warp, lane, xv);
             if (two) slice_load_x(p, m + 1, s, warp, lane, xv2);
             slice_transform_rows(s, xv, tbuf, warp, lane);
             __syncthreads();
@@ -641,8 +685,8 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
                         tile_dot1(LutPlain{lut}, rb[d], rs[d], base_off, v0);
                     }
                     const int tn0 = t0 + kDecodeWarps * RING, tn1 = t1 + kDecodeWarps * RING;
-                    if (tn0 < tb) load_tile(p, s, tn0, lane, rb[d], rs[d]);
-                    if (tn1 < tb) load_tile(p, s, tn1, lane, rb[d + 1], rs[d + 1]);
+                    if (tn0 < tb) load_tile<!TWO>(p, s, tn0, lane, rb[d], rs[d]);
+                    if (tn1 < tb) load_tile<!TWO>(p, s, tn1, lane, rb[d + 1], rs[d + 1]);
                     put(m, t0, v0);
                     if (t1 < tb) put(m, t1, v1);
                     if (two) {
