@@ -57,8 +57,10 @@
 //    of the first part of its weight share.
 //  * Every instruction before the lookups is on a call's critical path (the
 //    CTAs that start last, on SMs whose previous CTA ended last, set the
-//    call's time), so the tile-range split and the partial-sum placement use
-//    32-bit arithmetic and no runtime division.
+//    call's time), so the tile-range split, the partial-sum placement and the
+//    cluster finish use no runtime division (the launcher passes the split
+//    and ceil(2^32 / S)), and the one-token instance forms the addresses of x
+//    before the wait.
 #include <cuda_fp16.h>
 
 #include "bitlin_internal.cuh"
