@@ -9,7 +9,8 @@
 //
 // How (GB300 design):
 //  * Work unit = (slice s of 512 weights along K) x (tile t of 32 rows).  A CTA
-//    (16 warps, one per SM) owns one slice and a contiguous range of tiles.
+//    (one per SM: 16 warps, or 24 with a 2-deep ring for cluster shapes of at
+//    most 48 tiles per CTA) owns one slice and a contiguous range of tiles.
 //    Split-K: when the S slices of a tile range fit a thread-block cluster
 //    (S <= 16) and their partial sums fit shared memory, the S CTAs form a
 //    cluster, keep their partials in shared memory and sum them through
@@ -80,6 +81,12 @@ constexpr int kLut2Off = (kDecodeSmem + 127) & ~127;
 constexpr int kPbufOff = (kDecodeSmem + 15) & ~15;  // M = 1
 constexpr int kPbufOff2 = kLut2Off + kLutBytes;     // M >= 2
 constexpr int kMaxClusterSlices = 16;
+// Warps of the wide one-token CTA (cluster split-K with at most 48 tiles per
+// CTA): two tiles per warp at most, a 2-deep register ring, 80 registers per
+// thread (warps are dealt round robin to the SM's four sub-partitions of
+// 16,384 registers: 6 x 32 x 80 fit, 6 x 32 x 96 do not launch).  Warps
+// 0-15 run the x / transform / table prologue; all of them look up.
+constexpr int kWideWarps = 24;
 // Aligned-table layout (M = 1): the allocation holds a pad of up to 64 KB,
 // the table at the first 64 KB-aligned shared address, and the transpose
 // buffer, slice and partial sums (below the table when the pad holds them,
@@ -479,14 +486,15 @@ constexpr int kDecodeRegs = BITLIN_DECODE_REGS;
 __device__ __forceinline__ int div_s(const DecodeParams& p, int v) { return (int)__umulhi((unsigned)v, p.s_mul); }
 __device__ __forceinline__ int cluster_slots(const DecodeParams& p, int ntile) { return div_s(p, ntile + p.S - 1); }
 
-__device__ __forceinline__ void cluster_finish(const DecodeParams& p, int ta, int tb, int rank, const float* pbuf)
+__device__ __forceinline__ void cluster_finish(const DecodeParams& p, int ta, int tb, int rank, const float* pbuf,
+                                               int threads)
 {
     ptx::cluster_sync();
     const int ntile = tb - ta, S = p.S, LT = cluster_slots(p, ntile);
     const int mine = ntile > rank ? div_s(p, ntile - rank + S - 1) : 0;  // tiles rank, rank + S, ...
     const int stride = LT * kTileRows;
     for (int m = 0; m < p.M; ++m)
-    for (int i = (int)threadIdx.x; i < mine * kTileRows; i += kDecodeThreads) {
+    for (int i = (int)threadIdx.x; i < mine * kTileRows; i += threads) {
         const int slot = i >> 5, lane = i & 31;
         const float* src = pbuf + (m * S * LT + slot) * kTileRows + lane;
         // All S loads in flight at once, then the sum in slice order.
@@ -508,11 +516,12 @@ __device__ __forceinline__ void cluster_finish(const DecodeParams& p, int ta, in
 // TWO: tokens are taken two at a time (M >= 2), with a 2-deep register ring so
 // that both tokens' accumulators fit the register budget; M = 1 keeps the
 // 4-deep ring.  AL (M = 1 only): the table at a 64 KB-aligned shared address.
-template <bool TWO, bool AL>
-__global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p)
+template <bool TWO, bool AL, int NW>
+__global__ void __maxnreg__(NW == kDecodeWarps ? kDecodeRegs : 80) bitlin_decode_gemv(const DecodeParams p)
 {
+    static_assert(NW == kDecodeWarps || (!TWO && AL), "more warps only for one token with the aligned table");
     static_assert(!(TWO && AL), "the aligned table is for one token at a time");
-    constexpr int RING = TWO ? 2 : kRing;
+    constexpr int RING = TWO || NW != kDecodeWarps ? 2 : kRing;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* lut = smem;
     float* tbuf = reinterpret_cast<float*>(smem + kLutBytes);
@@ -530,6 +539,7 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
     float* xs = tbuf + 16 * kPad;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool pro = NW == kDecodeWarps || warp < kDecodeWarps;  // the warps of the x / transform / table prologue
     // Units owned by this CTA, [u0, u1) in slice-major order.  With
     // ctas_per_slice > 0 every CTA stays inside one slice (one table build);
     // otherwise (more slices than CTAs) the units are split evenly.
@@ -587,10 +597,10 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
         const int s = s0, ta = u0 - s * p.T, tb = min(p.T, ta + (u1 - u0));
 #pragma unroll
         for (int d = 0; d < RING; ++d) {
-            const int t = ta + warp + kDecodeWarps * d;
+            const int t = ta + warp + NW * d;
             if (u0 < u1 && t < tb) load_tile<!TWO>(p, s, t, lane, rb[d], rs[d]);
         }
-        if (u0 < u1) {
+        if (pro && u0 < u1) {
             slice_load_signs(p, s, warp, lane, xv);
             slice_prefetch_x(p, 0, s, warp, lane);
             if (!TWO) slice_x_ptrs(p, 0, s, warp, lane, xptr);
@@ -613,10 +623,10 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
             const bool first = preloaded;
             if (!preloaded) __syncthreads();  // the previous tables and buffers are no longer read
             if (!preloaded) {
-                slice_load_signs(p, s, warp, lane, xv);
+                if (pro) slice_load_signs(p, s, warp, lane, xv);
 #pragma unroll
                 for (int d = 0; d < RING; ++d) {
-                    const int t = ta + warp + kDecodeWarps * d;
+                    const int t = ta + warp + NW * d;
                     if (t < tb) load_tile<!TWO>(p, s, t, lane, rb[d], rs[d]);
                 }
             }
@@ -624,14 +634,16 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
             float xv2[4 * kRowsPerWarp];
 #pragma unroll
             for (int i = 0; i < 4 * kRowsPerWarp; ++i) xv2[i] = xv[i];  // the signs
-            if (!TWO && first) slice_load_x_at(p, xptr, xv);
-            else slice_load_x(p, m, s, warp, lane, xv);
-            if (two) slice_load_x(p, m + 1, s, warp, lane, xv2);
-            slice_transform_rows(s, xv, tbuf, warp, lane);
+            if (pro) {
+                if (!TWO && first) slice_load_x_at(p, xptr, xv);
+                else slice_load_x(p, m, s, warp, lane, xv);
+                if (two) slice_load_x(p, m + 1, s, warp, lane, xv2);
+                slice_transform_rows(s, xv, tbuf, warp, lane);
+            }
             __syncthreads();
-            slice_transform_cols(tbuf, xs, warp, lane);
+            if (pro) slice_transform_cols(tbuf, xs, warp, lane);
             __syncthreads();
-            build_tables(xs, lut, warp, lane);
+            if (pro) build_tables(xs, lut, warp, lane);
             if (two) {
                 __syncthreads();  // tbuf and xs are free again
                 slice_transform_rows(s, xv2, tbuf, warp, lane);
@@ -668,8 +680,8 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
                 bool more = true;
 #pragma unroll
                 for (int d = 0; d < RING; d += 2) {
-                    const int t0 = ta + warp + kDecodeWarps * (j0 + d);
-                    const int t1 = t0 + kDecodeWarps;
+                    const int t0 = ta + warp + NW * (j0 + d);
+                    const int t1 = t0 + NW;
                     if (t0 >= tb) {
                         more = false;
                         break;
@@ -686,7 +698,7 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
                     } else {
                         tile_dot1(LutPlain{lut}, rb[d], rs[d], base_off, v0);
                     }
-                    const int tn0 = t0 + kDecodeWarps * RING, tn1 = t1 + kDecodeWarps * RING;
+                    const int tn0 = t0 + NW * RING, tn1 = t1 + NW * RING;
                     if (tn0 < tb) load_tile<!TWO>(p, s, tn0, lane, rb[d], rs[d]);
                     if (tn1 < tb) load_tile<!TWO>(p, s, tn1, lane, rb[d + 1], rs[d + 1]);
                     put(m, t0, v0);
@@ -699,7 +711,7 @@ __global__ void __maxnreg__(kDecodeRegs) bitlin_decode_gemv(const DecodeParams p
                 if (!more) break;
             }
         }
-        if (p.cluster) cluster_finish(p, ta, tb, rank, pbuf);
+        if (p.cluster) cluster_finish(p, ta, tb, rank, pbuf, 32 * NW);
     }
     if (!triggered) pdl_launch_dependents();
 }
@@ -764,8 +776,8 @@ int max_clusters(int S, int num_sms)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0, per_sm = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, bitlin_decode_gemv<false, false>, &cfg) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bitlin_decode_gemv<false, false>, kDecodeThreads,
+    if (cudaOccupancyMaxActiveClusters(&n, bitlin_decode_gemv<false, false, kDecodeWarps>, &cfg) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bitlin_decode_gemv<false, false, kDecodeWarps>, kDecodeThreads,
                                                       kPbufOff + kPbufBytes) != cudaSuccess) {
         (void)cudaGetLastError();
         n = 0;
@@ -788,7 +800,8 @@ cudaError_t configure_decode()
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e == cudaSuccess && g_max_smem < kPbufOff2) e = cudaErrorInvalidConfiguration;
-    for (auto k : {bitlin_decode_gemv<false, false>, bitlin_decode_gemv<false, true>, bitlin_decode_gemv<true, false>}) {
+    for (auto k : {bitlin_decode_gemv<false, false, kDecodeWarps>, bitlin_decode_gemv<false, true, kDecodeWarps>,
+                   bitlin_decode_gemv<false, true, kWideWarps>, bitlin_decode_gemv<true, false, kDecodeWarps>}) {
         if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g_max_smem);
         if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     }
@@ -800,13 +813,13 @@ cudaError_t configure_decode()
 // split-K through the scratch and bitlin_decode_reduce), whether the table is
 // 64 KB-aligned, and q's launcher fields.
 struct DecodeShape {
-    int grid, smem, cluster, aligned;
+    int grid, smem, cluster, aligned, wide;
 };
 
 DecodeShape decode_shape(const DecodeParams& p, int num_sms, DecodeParams& q)
 {
     q = p;
-    DecodeShape d{0, p.M >= 2 ? kPbufOff2 : kDecodeSmem, 0, 0};  // two tables from M = 2
+    DecodeShape d{0, p.M >= 2 ? kPbufOff2 : kDecodeSmem, 0, 0, 0};  // two tables from M = 2
     int pbytes = 0;  // cluster split-K partial sums per CTA
     q.cluster = 0;
     q.s_mul = 0xFFFFFFFFu / (unsigned)p.S + 1u;  // ceil(2^32 / S); S = K / 512 >= 2
@@ -849,6 +862,10 @@ DecodeShape decode_shape(const DecodeParams& p, int num_sms, DecodeParams& q)
     if (p.M == 1 && pbytes <= kAlMaxPbuf && kAlSmemBase + pbytes <= g_max_smem) {
         d.aligned = 1;
         d.smem = kAlSmemBase + pbytes;
+        // Cluster split-K with at most two tiles per warp of the wide CTA (every
+        // tile in its ring): ffn_gate 5.64 -> 5.57 us.  The scratch path measured
+        // slower with it (ffn_down 7.99 against 8.22 us), so it keeps 16 warps.
+        if (q.cluster && q.split_q + (q.split_r > 0 ? 1 : 0) <= 2 * kWideWarps) d.wide = 1;
     }
     return d;
 }
@@ -882,14 +899,15 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kDecodeThreads);
+    cfg.blockDim = dim3(d.wide ? 32 * kWideWarps : kDecodeThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = cluster ? 2 : 1;
-    e = p.M >= 2   ? cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<true, false>, q)
-        : d.aligned ? cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<false, true>, q)
-                    : cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<false, false>, q);
+    e = p.M >= 2   ? cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<true, false, kDecodeWarps>, q)
+        : d.wide    ? cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<false, true, kWideWarps>, q)
+        : d.aligned ? cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<false, true, kDecodeWarps>, q)
+                    : cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<false, false, kDecodeWarps>, q);
     if (e != cudaSuccess || q.cluster) return e;
     // Scratch split-K: the sum over the slices, launched as the GEMV's dependent.
     const long long outs = (long long)p.M * p.N;
