@@ -14,7 +14,9 @@
 //    Split-K: when the S slices of a tile range fit a thread-block cluster
 //    (S <= 16) and their partial sums fit shared memory, the S CTAs form a
 //    cluster, keep their partials in shared memory and sum them through
-//    distributed shared memory (cluster_finish).  Otherwise the partials land
+//    distributed shared memory (cluster_finish; a first cluster barrier phase,
+//    arrived at on entry and waited on before the first remote store, makes
+//    sure every CTA of the cluster has started).  Otherwise the partials land
 //    in a scratch array and a second kernel (bitlin_decode_reduce, chained by
 //    programmatic dependent launch) sums every output over the slices with
 //    one thread each.  Both sum in the fixed order s = 0..S-1 (deterministic).
@@ -540,6 +542,10 @@ __global__ void __maxnreg__(NW == kDecodeWarps ? kDecodeRegs : 80) bitlin_decode
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool pro = NW == kDecodeWarps || warp < kDecodeWarps;  // the warps of the x / transform / table prologue
+    // Cluster split-K writes into the other CTAs' shared memory: every thread
+    // signals that its CTA has started, and waits for the whole cluster's
+    // signal before the first of those writes (long since complete by then).
+    if (p.cluster) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     // Units owned by this CTA, [u0, u1) in slice-major order.  With
     // ctas_per_slice > 0 every CTA stays inside one slice (one table build);
     // otherwise (more slices than CTAs) the units are split evenly.
@@ -584,7 +590,7 @@ __global__ void __maxnreg__(NW == kDecodeWarps ? kDecodeRegs : 80) bitlin_decode
         prefetch_l2(p.bits + (size_t)u0 * 128, (size_t)pu * 2048, threadIdx.x);
         prefetch_l2(p.scales + (size_t)u0 * 32, (size_t)pu * 256, (threadIdx.x + 128) % kDecodeThreads);
     }
-    // Before the wait: this warp's first tiles (ta + warp + warps * j, j < kRing) and
+    // Before the wait: this warp's first tiles (ta + warp + NW * j, j < RING) and
     // the signs of the first segment, whose latency then overlaps the wait, and
     // the L2 hint for x.
     uint4 rb[RING][4];
@@ -658,6 +664,7 @@ __global__ void __maxnreg__(NW == kDecodeWarps ? kDecodeRegs : 80) bitlin_decode
             if (!triggered) {
                 pdl_launch_dependents();
                 triggered = true;
+                if (p.cluster) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
             }
             // Partial sums.  Scratch path: token mm, tile t, lane ->
             // partials[s][mm][t * 32 + lane].  Cluster path: into the owner's shared
