@@ -186,23 +186,78 @@ def roofline(w: synth.Workload, s_per_step: float, peaks: dict, peak_kind: str, 
             "flops_per_launch": flops, "traffic": traffic_record(kernel, w.name)}
 
 
+def cpu_model() -> str:
+    """The host CPU's model string (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
+
+
+def timed_calls(fn, seconds: float, min_calls: int = 1):
+    """Call fn() until `seconds` have passed (at least min_calls times): (calls, seconds)."""
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds and n >= min_calls:
+            return n, el
+
+
+def oracle_rates(fn, tokens_per_call: float, seconds: float) -> dict:
+    """The oracle call fn, as it stands, on every host core for about `seconds` and on one
+    thread for about a third of that: tokens/s, cores, both times per call, the CPU model."""
+    import oracle
+
+    cores = oracle.max_threads()
+    n, el = timed_calls(fn, seconds)
+    oracle.set_threads(1)
+    try:
+        n1, el1 = timed_calls(fn, seconds / 3)
+    finally:
+        oracle.set_threads(cores)
+    return {"value": n * tokens_per_call / el, "cores": cores, "calls": n, "seconds": el,
+            "ms_per_call_all_cores": 1e3 * el / n, "ms_per_call_one_thread": 1e3 * el1 / n1,
+            "one_thread_tokens_per_s": n1 * tokens_per_call / el1, "cpu_model": cpu_model()}
+
+
 def cpu_baseline(w: synth.Workload, inputs, seconds: float):
-    """The oracle, as it stands, on the host cores: whole calls for about `seconds`."""
+    """The oracle, as it stands, on the host cores: on every core for about `seconds`, and on
+    one thread for a third of that.  A call covers every output row when a whole call takes
+    at most a quarter of `seconds` on all cores; otherwise the leading rows that take about a
+    twentieth (tokens/s then counts the fraction of each token's rows a call computes)."""
     import oracle
 
     oracle.build()
     bits, scales, signs, x = inputs
-    n = 0
+    probe = np.arange(min(64, w.N))
     t0 = time.perf_counter()
-    while True:
-        oracle.forward(bits, scales, signs, w.perm, x)
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": n * w.M / el, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"{n} whole oracle calls (M={w.M}, K={w.K}, N={w.N}) in {el:.1f} s, "
-                      f"f64, OpenMP over output rows"}
+    oracle.forward(bits, scales, signs, w.perm, x, probe)
+    est = (time.perf_counter() - t0) * w.N / probe.size
+    rows = w.N if est <= seconds / 4 else max(1, min(w.N, int(w.N * seconds / 20 / est)))
+    sel = None if rows == w.N else np.arange(rows)
+    r = oracle_rates(lambda: oracle.forward(bits, scales, signs, w.perm, x, sel), w.M * rows / w.N, seconds)
+    what = "whole oracle calls" if rows == w.N else f"oracle calls on the first {rows} of {w.N} output rows"
+    return {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+            "cpu_model": r["cpu_model"], "ms_per_call_all_cores": r["ms_per_call_all_cores"],
+            "ms_per_call_one_thread": r["ms_per_call_one_thread"],
+            "one_thread_value": r["one_thread_tokens_per_s"],
+            "sample": f"{r['calls']} {what} (M={w.M}, K={w.K}, N={w.N}) in {r['seconds']:.1f} s "
+                      f"on {r['cores']} threads, then the same calls on one thread; f64, OpenMP over output rows"}
 
 
 def run_reference(args, w: synth.Workload):
@@ -257,6 +312,7 @@ def run_reference(args, w: synth.Workload):
         "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "perm": w.perm,
                    "rows_per_step": rows},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                         "cpu_model": cpu_model(),
                          "sample": f"{args.steps} steps of {rows} output rows each (rotation once per token)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -268,29 +324,31 @@ EMBED_METRIC = "embedding lookups/s with the inverse rotation (1-bit WHT-folded 
 LMHEAD_METRIC = "LM head tokens/s and weight GB/s (1-bit WHT-folded 248320x5120 product + argmax)"
 
 
-def timed_graph(step, stream, steps: int, warmup: int, pg, dev):
-    """Warm up, capture `step` calls in CUDA graphs, replay exactly `steps` calls between a
-    barrier and device synchronizes; CUDA events on `stream`.  Returns (ms, clocks)."""
+def flush_l2(dev, l2_bytes: int, stream):
+    """Overwrite a buffer twice the L2 size on `stream`, so that nothing a warm-up left in L2
+    is still there when the timed region starts."""
     import torch
 
     with torch.cuda.stream(stream):
-        for i in range(warmup):
-            step(i)
+        buf = torch.empty(2 * l2_bytes // 4 + 1, dtype=torch.float32, device=dev)
+        buf.zero_()
     stream.synchronize()
-    chunk = min(256, max(1, steps))
+    del buf
 
-    def capture(n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(n):
-                    step(i)
-        return g
 
-    full, rem = divmod(steps, chunk)
-    g_chunk = capture(chunk) if full else None
-    g_rem = capture(rem) if rem else None
-    sampler = ClockSampler(torch.cuda.current_device())
+# Device-side delay before the first timed event (cycles of the SM clock, about 1 ms): the
+# stream is then busy while the host enqueues the event and the graph replays, so the timed
+# region holds device work only, not the host's launch latency.
+HOLD_CYCLES = 2_000_000
+
+
+def run_timed(replays, stream, pg, dev, gpu_index: int):
+    """The timed region: a barrier and a device synchronize, a device-side hold, an event,
+    `replays` (graphs, each already replayed once), an event, a device synchronize and a
+    barrier.  nvidia-smi samples the clocks throughout.  Returns (ms over ranks, clocks)."""
+    import torch
+
+    sampler = ClockSampler(gpu_index)
     sampler.start()
     time.sleep(0.3)
     if pg:
@@ -298,18 +356,57 @@ def timed_graph(step, stream, steps: int, warmup: int, pg, dev):
     torch.cuda.synchronize(dev)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        torch.cuda._sleep(HOLD_CYCLES)
         ev0.record(stream)
-        for _ in range(full):
-            g_chunk.replay()
-        if g_rem:
-            g_rem.replay()
+        for g in replays:
+            g.replay()
         ev1.record(stream)
     torch.cuda.synchronize(dev)
     if pg:
         pg.barrier()
     clocks = sampler.stop()
     return max_over_ranks(ev0.elapsed_time(ev1), pg, dev), clocks
+
+
+def capture_steps(step, stream, steps: int, chunk: int):
+    """CUDA graphs of `chunk` consecutive calls (as many as fit in `steps`) and one of the
+    remainder; every graph is replayed once before it is returned, so that the timed
+    region never holds a graph's first launch (its upload).  Returns the replay list whose
+    calls add up to exactly `steps`."""
+    import torch
+
+    def capture(n, first):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(first, first + n):
+                    step(i)
+        return g
+
+    full, rem = divmod(steps, chunk)
+    g_chunk = capture(chunk, 0) if full else None
+    g_rem = capture(rem, full * chunk) if rem else None
+    with torch.cuda.stream(stream):
+        for g in (g_chunk, g_rem):
+            if g is not None:
+                g.replay()
+    stream.synchronize()
+    return [g_chunk] * full + ([g_rem] if g_rem is not None else [])
+
+
+def timed_graph(step, stream, steps: int, warmup: int, pg, dev, chunk: int = 256):
+    """Warm up, capture `step` calls in CUDA graphs (each replayed once), flush L2, replay
+    exactly `steps` calls in the timed region (run_timed).  Returns (ms, clocks)."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+    stream.synchronize()
+    replays = capture_steps(step, stream, steps, min(chunk, max(1, steps)))
+    flush_l2(dev, torch.cuda.get_device_properties(dev).L2_cache_size, stream)
+    return run_timed(replays, stream, pg, dev, torch.cuda.current_device())
 
 
 def run_op(args, ws, rank, local, pg):
@@ -499,18 +596,13 @@ def run_op(args, ws, rank, local, pg):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "api": "python binding, pinned host buffers"},
     }
     if not args.no_cpu_baseline:
-        import oracle
-
-        fn = cpu_call()
-        n, t0 = 0, time.perf_counter()
-        while True:
-            fn()
-            n += 1
-            el = time.perf_counter() - t0
-            if el >= args.cpu_seconds:
-                break
-        line["cpu_baseline"] = {"value": n * M / el, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-                                "sample": f"{n} whole oracle calls in {el:.1f} s, f64"}
+        r = oracle_rates(cpu_call(), M, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+                                "cpu_model": r["cpu_model"], "ms_per_call_all_cores": r["ms_per_call_all_cores"],
+                                "ms_per_call_one_thread": r["ms_per_call_one_thread"],
+                                "one_thread_value": r["one_thread_tokens_per_s"],
+                                "sample": f"{r['calls']} whole oracle calls in {r['seconds']:.1f} s on "
+                                          f"{r['cores']} threads, then whole calls on one thread; f64"}
     print(json.dumps(line), flush=True)
 
 
@@ -568,44 +660,14 @@ def main():
             layers[i % R](xd, out=yd, stream=stream)
     stream.synchronize()
 
-    chunk = R * max(1, 256 // R)
-    def capture(ncalls):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(ncalls):
-                    layers[i % R](xd, out=yd, stream=stream)
-        return g
+    # Graphs of whole cycles through the R copies; step i uses copy i % R, so a call
+    # re-reads a copy only after R - 1 others (R * the matrix size >= 4x L2).
+    def step(i):
+        layers[i % R](xd, out=yd, stream=stream)
 
-    full, rem = divmod(args.steps, chunk)
-    g_chunk = capture(chunk) if full else None
-    g_rem = capture(rem) if rem else None
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            if g_chunk:
-                g_chunk.replay()
-    stream.synchronize()
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize(dev)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):  # replay() launches on the current stream
-        ev0.record(stream)
-        for _ in range(full):
-            g_chunk.replay()
-        if g_rem:
-            g_rem.replay()
-        ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    if pg:
-        pg.barrier()
-    clocks = sampler.stop()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
+    replays = capture_steps(step, stream, args.steps, R * max(1, 256 // R))
+    flush_l2(dev, l2, stream)
+    ms, clocks = run_timed(replays, stream, pg, dev, local)
     assert layers[0].get_error() == 0
 
     # End to end through the host-buffer entry point (pinned host memory).
@@ -649,7 +711,10 @@ def main():
                    "kernel_path": {1: "decode GEMV (f32)", 2: "tcgen05, bf16 activations",
                                    3: "tcgen05, three exact bf16 digits, f32 accumulation"}[path],
                    "weight_copies": R, "weight_set_bytes": R * wbytes,
-                   "l2": f"inputs larger than L2: {R} distinct weight copies ({R * wbytes / 1e6:.0f} MB) cycled",
+                   "l2": f"inputs larger than L2: {R} distinct weight copies ({R * wbytes / 1e6:.0f} MB) cycled; "
+                         f"L2 flushed before the timed region",
+                   "timing": "CUDA events on the launching stream around graph replays that were each replayed "
+                             "once before; the stream is held by a device-side delay while the host enqueues them",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "weight_gbs": w.weight_bytes() / s_per_step / 1e9,
         "hbm_frac_of_8tbs": achieved / 8000.0,

@@ -135,7 +135,11 @@ DecodeParams decode_params(bitlin_t h, const float* x, int M, float* y, int swig
 
 bitlin_status run_decode(bitlin_t h, const float* x, int M, float* y, cudaStream_t s, int swiglu = 0)
 {
-    cudaError_t e = ensure_partials(h, M);
+    // The split-K scratch only when the call sums its slices outside a cluster
+    // (two kernels); the cluster path keeps its partial sums in shared memory.
+    int kernels = 0;
+    cudaError_t e = bitlin_decode_kernels(decode_params(h, x, M, y, swiglu), h->num_sms, &kernels);
+    if (e == cudaSuccess && kernels == 2) e = ensure_partials(h, M);
     if (e != cudaSuccess) return from_cuda(h, e);
     return from_cuda(h, bitlin_launch_decode(decode_params(h, x, M, y, swiglu), h->num_sms, s));
 }
@@ -469,8 +473,6 @@ bitlin_status bitlin_argmax(bitlin_t h, const float* x, int M, float* logits, in
     if (!y) {
         if (!h->logits || h->logits_M < M) {
             free_dev(h->logits);
-    free_dev(h->amax_cand);
-    free_dev(h->amax_tickets);
             h->logits_M = 0;
             cudaError_t e = cudaMalloc(&h->logits, (size_t)M * h->N * sizeof(float));
             if (e != cudaSuccess) return from_cuda(h, e);
@@ -484,8 +486,8 @@ bitlin_status bitlin_argmax(bitlin_t h, const float* x, int M, float* logits, in
         h->amax_M = 0;
         cudaError_t e = cudaMalloc(&h->amax_cand, bitlin_argmax_scratch_bytes(M));
         if (e == cudaSuccess) e = cudaMalloc(&h->amax_tickets, (size_t)M * sizeof(unsigned));
-        if (e == cudaSuccess) e = cudaMemset(h->amax_tickets, 0, (size_t)M * sizeof(unsigned));
-        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        // Zeroed in stream order: the pick kernels on this stream see zero tickets.
+        if (e == cudaSuccess) e = cudaMemsetAsync(h->amax_tickets, 0, (size_t)M * sizeof(unsigned), s);
         if (e != cudaSuccess) return from_cuda(h, e);
         h->amax_M = M;
     }

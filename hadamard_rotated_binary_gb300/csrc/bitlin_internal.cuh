@@ -4,9 +4,39 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "bitlin.h"
 
 namespace bitlin_impl {
+
+// ---- per-device set-up -----------------------------------------------------
+// Kernel attributes (cudaFuncSetAttribute) and occupancy queries apply to the
+// device that is current when they run, so the launchers set them up once per
+// device ordinal, under a lock, with that device current.
+constexpr int kMaxDevices = 64;
+
+struct PerDeviceOnce {
+    std::atomic<int> done[kMaxDevices] = {};
+    std::mutex mu;
+
+    // Runs fn(dev) once for the current device (again after a failure);
+    // *dev receives the current device's ordinal.
+    template <class F>
+    cudaError_t run(int* dev, F&& fn)
+    {
+        cudaError_t e = cudaGetDevice(dev);
+        if (e != cudaSuccess) return e;
+        if (*dev < 0 || *dev >= kMaxDevices) return cudaErrorInvalidDevice;
+        if (done[*dev].load(std::memory_order_acquire)) return cudaSuccess;
+        std::lock_guard<std::mutex> lock(mu);
+        if (done[*dev].load(std::memory_order_relaxed)) return cudaSuccess;
+        e = fn(*dev);
+        if (e == cudaSuccess) done[*dev].store(1, std::memory_order_release);
+        return e;
+    }
+};
 
 // ---- decode layout -------------------------------------------------------
 // The decode GEMV works on units of (32 rows) x (512 weights along K): a

@@ -761,16 +761,21 @@ namespace {
 // sums (the vocabulary matrix, 248,320 rows over 13 clusters, needs 76 KB).
 constexpr int kPbufBytes = 96 * 1024;
 
-// Clusters of S CTAs that one call may use, by S: the clusters that can be
-// resident at once divided by the CTAs that fit on an SM, so that when two
-// fit, the next call's CTAs find room beside this call's and start their
-// weight prefetch early.  0 = not queried yet, -1 = none.
-int g_max_clusters[kMaxClusterSlices + 1];
-int g_max_smem = 0;  // opt-in shared memory per block of the device
+// Per device: the opt-in shared memory per block, and the clusters of S CTAs
+// that one call may use, by S: the clusters that can be resident at once
+// divided by the CTAs that fit on an SM, so that when two fit, the next call's
+// CTAs find room beside this call's and start their weight prefetch early
+// (0 = none).  Set up once per device: kernel attributes apply to the device
+// that is current when they are set.
+struct DecodeDevice {
+    int max_smem = 0;
+    int max_clusters[kMaxClusterSlices + 1] = {};
+};
+DecodeDevice g_decode_dev[kMaxDevices];
+PerDeviceOnce g_decode_once;
 
-int max_clusters(int S, int num_sms)
+int query_max_clusters(int S, int num_sms)
 {
-    if (g_max_clusters[S] != 0) return g_max_clusters[S];
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = S;
@@ -790,29 +795,29 @@ int max_clusters(int S, int num_sms)
         n = 0;
     }
     if (per_sm > 1) n /= per_sm;
-    if (n < 1) n = -1;
-    g_max_clusters[S] = n;
-    return n;
+    return n < 1 ? 0 : n;
 }
 
-}  // namespace
-
-namespace {
-
-cudaError_t configure_decode()
+// The current device's decode set-up (kernel attributes, opt-in shared memory,
+// cluster capacities), done once per device.
+cudaError_t configure_decode(const DecodeDevice** out)
 {
-    static bool configured = false;
-    if (configured) return cudaSuccess;
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e == cudaSuccess && g_max_smem < kPbufOff2) e = cudaErrorInvalidConfiguration;
-    for (auto k : {bitlin_decode_gemv<false, false, kDecodeWarps>, bitlin_decode_gemv<false, true, kDecodeWarps>,
-                   bitlin_decode_gemv<false, true, kWideWarps>, bitlin_decode_gemv<true, false, kDecodeWarps>}) {
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g_max_smem);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    }
-    if (e == cudaSuccess) configured = true;
+    cudaError_t e = g_decode_once.run(&dev, [](int d) {
+        DecodeDevice& c = g_decode_dev[d];
+        int sms = 0;
+        cudaError_t r = cudaDeviceGetAttribute(&c.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
+        if (r == cudaSuccess && c.max_smem < kPbufOff2) r = cudaErrorInvalidConfiguration;
+        for (auto k : {bitlin_decode_gemv<false, false, kDecodeWarps>, bitlin_decode_gemv<false, true, kDecodeWarps>,
+                       bitlin_decode_gemv<false, true, kWideWarps>, bitlin_decode_gemv<true, false, kDecodeWarps>}) {
+            if (r == cudaSuccess) r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, c.max_smem);
+            if (r == cudaSuccess) r = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        }
+        for (int S = 2; r == cudaSuccess && S <= kMaxClusterSlices; ++S) c.max_clusters[S] = query_max_clusters(S, sms);
+        return r;
+    });
+    *out = e == cudaSuccess ? &g_decode_dev[dev] : nullptr;
     return e;
 }
 
@@ -823,7 +828,7 @@ struct DecodeShape {
     int grid, smem, cluster, aligned, wide;
 };
 
-DecodeShape decode_shape(const DecodeParams& p, int num_sms, DecodeParams& q)
+DecodeShape decode_shape(const DecodeParams& p, int num_sms, const DecodeDevice& dc, DecodeParams& q)
 {
     q = p;
     DecodeShape d{0, p.M >= 2 ? kPbufOff2 : kDecodeSmem, 0, 0, 0};  // two tables from M = 2
@@ -833,13 +838,13 @@ DecodeShape decode_shape(const DecodeParams& p, int num_sms, DecodeParams& q)
     // Split-K across a cluster when the slices fit one (S <= 16) and the
     // partial sums fit shared memory; else through the global scratch.
     if (p.allow_cluster && p.S <= kMaxClusterSlices) {
-        const int maxc = max_clusters(p.S, num_sms);
+        const int maxc = dc.max_clusters[p.S];
         if (maxc > 0) {
             const int ncl = maxc < p.T ? maxc : p.T;
             const int lt = ((p.T + ncl - 1) / ncl + p.S - 1) / p.S;  // slots per CTA
             const long long pb = (long long)p.M * p.S * lt * kTileRows * 4;
             const int poff = p.M >= 2 ? kPbufOff2 : kPbufOff;
-            if (pb <= kPbufBytes && poff + pb <= g_max_smem) {
+            if (pb <= kPbufBytes && poff + pb <= dc.max_smem) {
                 q.cluster = 1;
                 q.ctas_per_slice = ncl;
                 d.grid = p.S * ncl;
@@ -866,7 +871,7 @@ DecodeShape decode_shape(const DecodeParams& p, int num_sms, DecodeParams& q)
     // One token: the aligned table when the partial sums are small (the
     // allocation covers the worst-case pad below the table).
     q.pbuf_bytes = pbytes;
-    if (p.M == 1 && pbytes <= kAlMaxPbuf && kAlSmemBase + pbytes <= g_max_smem) {
+    if (p.M == 1 && pbytes <= kAlMaxPbuf && kAlSmemBase + pbytes <= dc.max_smem) {
         d.aligned = 1;
         d.smem = kAlSmemBase + pbytes;
         // Cluster split-K with at most two tiles per warp of the wide CTA (every
@@ -881,19 +886,21 @@ DecodeShape decode_shape(const DecodeParams& p, int num_sms, DecodeParams& q)
 
 cudaError_t bitlin_decode_kernels(const DecodeParams& p, int num_sms, int* kernels)
 {
-    cudaError_t e = configure_decode();
+    const DecodeDevice* dc = nullptr;
+    cudaError_t e = configure_decode(&dc);
     if (e != cudaSuccess) return e;
     DecodeParams q;
-    *kernels = decode_shape(p, num_sms, q).cluster ? 1 : 2;
+    *kernels = decode_shape(p, num_sms, *dc, q).cluster ? 1 : 2;
     return cudaSuccess;
 }
 
 cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_t s)
 {
-    cudaError_t e = configure_decode();
+    const DecodeDevice* dc = nullptr;
+    cudaError_t e = configure_decode(&dc);
     if (e != cudaSuccess) return e;
     DecodeParams q;
-    const DecodeShape d = decode_shape(p, num_sms, q);
+    const DecodeShape d = decode_shape(p, num_sms, *dc, q);
     const int grid = d.grid, smem = d.smem, cluster = d.cluster;
 
     cudaLaunchAttribute attr[2];

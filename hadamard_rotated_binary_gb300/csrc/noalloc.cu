@@ -30,7 +30,6 @@ using namespace bitlin_impl;
 namespace {
 
 constexpr size_t kNoallocScratchBytes = (size_t)16 << 20;  // 16 MiB
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 

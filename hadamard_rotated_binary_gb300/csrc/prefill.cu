@@ -396,13 +396,14 @@ template <int BN, bool EXACT>
 cudaError_t launch(const PrefillParams& p, const void* tmap, const void* tmap_bits, int stall_test,
                    cudaStream_t s)
 {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(bitlin_tc_gemm<BN, EXACT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<BN>());
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    // Once per device (the attribute applies to the current device).
+    static PerDeviceOnce once;
+    int dev = 0;
+    cudaError_t ce = once.run(&dev, [](int) {
+        return cudaFuncSetAttribute(bitlin_tc_gemm<BN, EXACT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    smem_bytes<BN>());
+    });
+    if (ce != cudaSuccess) return ce;
     const int rows_b = EXACT ? 4 * p.M : p.M;
     const int gx = (p.N + kPrefillRows - 1) / kPrefillRows, gy = (rows_b + BN - 1) / BN;
     // Split K when the tiles would fill less than half of the SMs (tall-K,

@@ -3,15 +3,20 @@ device memory on their call path (a runtime that owns every device
 allocation, or a loop that must never enter the allocator because cudaMalloc
 can synchronize the device).
 
-Called through the C-ABI on the ffn_gate-shaped matrix, two calls in a row
-with different inputs, each compared with bitlin_forward on the same input
-within the decode tolerance.  Kept in a file that pytest collects last.
+Called through the C-ABI, two calls in a row with different inputs, on the
+ffn_gate shape at M = 1, 2 and 4 (the one-token and the two-tokens-per-pass
+kernels, both writing their partial sums into the fixed array), on the
+permuted ssm_out shape and on ffn_down (34 slices).  Each call is compared
+with the oracle within the decode tolerance and with bitlin_forward on the
+same input.  A fresh handle's first call must leave the device's free memory
+unchanged.  Kept in a file that pytest collects last.
 """
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 import synth
 
 torch = pytest.importorskip("torch")
@@ -22,37 +27,87 @@ DECODE_TOL = 1e-5
 
 
 def _rel(a, b):
-    a = a.double().cpu().numpy()
-    b = b.double().cpu().numpy()
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
     return float((np.linalg.norm(a - b, axis=1) / np.linalg.norm(b, axis=1)).max())
 
 
-def test_noalloc_matches_forward_on_two_calls_in_a_row():
+@pytest.fixture(scope="module")
+def hrb():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from hadamard_rotated_binary_gb300 import build as hbuild
 
     hbuild.build()
-    import hadamard_rotated_binary_gb300 as hrb
+    oracle.build()
+    import hadamard_rotated_binary_gb300 as m
 
-    L = hrb.lib()
-    w = synth.workload("ffn_gate")
+    return m
+
+
+def _layer(hrb, w):
     bits, scales, signs, _ = synth.make_inputs(w)
     layer = hrb.BitLinear(torch.from_numpy(bits.view(np.int32)).cuda(),
                           torch.from_numpy(scales.view(np.int16)).cuda(),
                           torch.from_numpy(signs).cuda(), w.perm)
+    return layer, (bits, scales, signs)
+
+
+def _noalloc(hrb, layer, x, M, N):
+    L = hrb.lib()
     stream = torch.cuda.current_stream()
+    y = torch.full((M, N), float("nan"), device="cuda")
+    st = L.bitlin_forward_noalloc(layer.handle, ctypes.c_void_p(x.data_ptr()), M,
+                                  ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+    return st, y
+
+
+@pytest.mark.parametrize("name,M", [("ffn_gate", 1), ("ffn_gate", 2), ("ffn_gate", 4), ("ssm_out", 1),
+                                    ("ffn_down", 1), ("ffn_down", 4)])
+def test_noalloc_matches_oracle_on_two_calls_in_a_row(hrb, name, M):
+    w = synth.workload(name, M)
+    layer, (bits, scales, signs) = _layer(hrb, w)
     for call, seed in enumerate((101, 202)):
-        x = torch.from_numpy(synth.random_x(seed, 1, w.K)).cuda()
-        ref = layer(x)
-        y = torch.full((1, w.N), float("nan"), device="cuda")
-        st = L.bitlin_forward_noalloc(layer.handle, ctypes.c_void_p(x.data_ptr()), 1,
-                                      ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+        xh = synth.random_x(seed, M, w.K)
+        x = torch.from_numpy(xh).cuda()
+        st, y = _noalloc(hrb, layer, x, M, w.N)
         assert st == hrb.BITLIN_OK, f"call {call}: status {st}"
         torch.cuda.synchronize()
         assert layer.get_error() == hrb.BITLIN_OK
-        assert torch.isfinite(y).all()
-        assert _rel(y, ref) <= DECODE_TOL, f"call {call}"
+        got = y.cpu().numpy()
+        assert np.isfinite(got).all()
+        ref = oracle.forward(bits, scales, signs, w.perm, xh)
+        assert _rel(got, ref) <= DECODE_TOL, f"call {call} against the oracle"
+        assert _rel(got, layer(x).cpu().numpy()) <= DECODE_TOL, f"call {call} against bitlin_forward"
+    layer.close()
+
+
+def test_noalloc_allocates_nothing_and_refuses_oversize(hrb):
+    L = hrb.lib()
+    w = synth.workload("ffn_gate", 4)
+    # A first call on another handle loads the library's kernels and its fixed
+    # array on this device; after that, a fresh handle's first call (which on
+    # bitlin_forward would allocate its split-K scratch) must allocate nothing.
+    # The warm-up runs both kernel instances (one token, two tokens per pass).
+    warm, _ = _layer(hrb, synth.workload("tiny"))
+    for m in (1, 4):
+        xw = torch.from_numpy(synth.random_x(7, m, 1024)).cuda()
+        assert _noalloc(hrb, warm, xw, m, 256)[0] == hrb.BITLIN_OK
+    torch.cuda.synchronize()
+    layer, (bits, scales, signs) = _layer(hrb, w)
+    xh = synth.random_x(303, 4, w.K)
+    x = torch.from_numpy(xh).cuda()
+    y = torch.empty((4, w.N), device="cuda")
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    st = L.bitlin_forward_noalloc(layer.handle, ctypes.c_void_p(x.data_ptr()), 4,
+                                  ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    assert st == hrb.BITLIN_OK
+    assert free1 == free0, f"free device memory changed by {free0 - free1} bytes"
+    assert _rel(y.cpu().numpy(), oracle.forward(bits, scales, signs, w.perm, xh)) <= DECODE_TOL
 
     # Sizes beyond the fixed scratch are refused before any launch.
     cap = L.bitlin_noalloc_scratch_bytes()
@@ -63,3 +118,4 @@ def test_noalloc_matches_forward_on_two_calls_in_a_row():
                                   ctypes.c_void_p(yb.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
     assert st == hrb.BITLIN_ESCRATCH
     layer.close()
+    warm.close()
