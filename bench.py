@@ -500,9 +500,12 @@ def run_op(args, ws, rank, local, pg):
         s_step = ms / 1e3 / args.steps
         algo = wbytes + 4 * M * K + 4 * M * N + 4 * K + 4 * M
         hpath, hk = heads[0].plan(M)
+        # One token through cluster split-K (one kernel): the pick is fused into the product's finish.
+        fused = hpath == hrb.PATH_DECODE and hk == 1
         if hpath == hrb.PATH_DECODE:
             roof = {"bound": "hbm", "achieved": algo / s_step / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "kernel": "bitlin_decode_gemv" + " + bitlin_decode_reduce" * (hk - 1) + " + bitlin_argmax_rows",
+                    "kernel": ("bitlin_decode_gemv (argmax fused)" if fused else
+                               "bitlin_decode_gemv" + " + bitlin_decode_reduce" * (hk - 1) + " + bitlin_argmax_rows"),
                     "bytes_per_launch": algo}
         else:
             digits = 3 if M < 64 else 1
@@ -513,7 +516,7 @@ def run_op(args, ws, rank, local, pg):
         metric, config = LMHEAD_METRIC, {"workload": "lm_head", "M": M, "N": N, "K": K, "weight_copies": R,
                                          "weight_set_bytes": R * wbytes,
                                          "l2": f"inputs larger than L2: {R} distinct copies cycled"}
-        launches, wgb = hk + 1, wbytes / s_step / 1e9
+        launches, wgb = hk + (0 if fused else 1), wbytes / s_step / 1e9
 
         def e2e_call(xh, yh):
             xd.copy_(xh, non_blocking=True)

@@ -17,16 +17,10 @@
 
 namespace {
 
-// Total order: NaN above everything, then the usual order; ties -> smaller index.
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi)
-{
-    const bool vn = v != v, bn = bv != bv;
-    if (vn != bn) return vn;
-    if (!vn && v != bv) return v > bv;
-    return i < bi;
-}
+using bitlin_impl::argmax_better;
+using bitlin_impl::kArgmaxSlots;
 
-constexpr int kChunks = 256;  // one chunk per CTA; the final pick reads one candidate per thread
+constexpr int kChunks = kArgmaxSlots;  // one chunk per CTA; the final pick reads one candidate per thread
 constexpr int kThreadsA = 256;
 static_assert(kChunks <= kThreadsA, "the final pick reads one candidate per thread");
 
@@ -36,7 +30,7 @@ __device__ __forceinline__ void warp_best(float& bv, int& bi)
     for (int o = 16; o; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (better(ov, oi, bv, bi)) {
+        if (argmax_better(ov, oi, bv, bi)) {
             bv = ov;
             bi = oi;
         }
@@ -81,7 +75,7 @@ __global__ void __launch_bounds__(kThreadsA) bitlin_argmax_rows(const float* __r
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int n = n0 + u * kThreadsA;
-            if (n < hi && better(v[u], n, bv, bi)) {
+            if (n < hi && argmax_better(v[u], n, bv, bi)) {
                 bv = v[u];
                 bi = n;
             }
@@ -120,4 +114,4 @@ cudaError_t bitlin_launch_argmax(const float* y, int M, int N, void* cand, unsig
     return cudaGetLastError();
 }
 
-size_t bitlin_argmax_scratch_bytes(int M) { return (size_t)M * kChunks * sizeof(float2); }
+size_t bitlin_argmax_scratch_bytes(int M) { return (size_t)M * kArgmaxSlots * sizeof(float2); }

@@ -130,6 +130,9 @@ DecodeParams decode_params(bitlin_t h, const float* x, int M, float* y, int swig
     p.cluster = 0;
     p.allow_cluster = 1;
     p.swiglu = swiglu;
+    p.ids = nullptr;
+    p.amax_cand = nullptr;
+    p.amax_tickets = nullptr;
     return p;
 }
 
@@ -490,6 +493,18 @@ bitlin_status bitlin_argmax(bitlin_t h, const float* x, int M, float* logits, in
         if (e == cudaSuccess) e = cudaMemsetAsync(h->amax_tickets, 0, (size_t)M * sizeof(unsigned), s);
         if (e != cudaSuccess) return from_cuda(h, e);
         h->amax_M = M;
+    }
+    // On the decode path with cluster split-K the GEMV picks the argmax in its
+    // finish; otherwise the scores are written first and a second kernel picks.
+    if (choose_path(h, M) == BITLIN_PATH_DECODE) {
+        DecodeParams p = decode_params(h, x, M, y, 0);
+        p.ids = ids;
+        p.amax_cand = static_cast<float2*>(h->amax_cand);
+        p.amax_tickets = h->amax_tickets;
+        int kernels = 0, fused = 0;
+        cudaError_t e = bitlin_decode_kernels(p, h->num_sms, &kernels, &fused);
+        if (e == cudaSuccess && fused) return from_cuda(h, bitlin_launch_decode(p, h->num_sms, s));
+        if (e != cudaSuccess) return from_cuda(h, e);
     }
     bitlin_status st = run_path(h, x, M, y, s, 0);
     if (st != BITLIN_OK) return st;

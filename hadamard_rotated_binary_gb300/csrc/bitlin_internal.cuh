@@ -76,12 +76,35 @@ struct DecodeParams {
     int M, N, K, S, T, perm;
     int ctas_per_slice;     // set by the launcher
     int split_q, split_r;   // set by the launcher: T = split_q * ctas_per_slice + split_r
-    unsigned s_mul;         // set by the launcher: ceil(2^32 / S), for division by S in the kernel
     int pbuf_bytes;         // set by the launcher: cluster split-K partial sums per CTA (bytes)
     int cluster;            // set by the launcher: 1 = split-K summed across a thread-block cluster
+    int csize;              // set by the launcher: CTAs per cluster, C = ceil(S / cspc)
+    int cspc;               // set by the launcher: slices per CTA of a cluster (rank r: r*cspc ...)
+    unsigned c_mul;         // set by the launcher: ceil(2^32 / C), for division by C in the kernel
     int allow_cluster;      // set by the caller: 0 keeps the split-K in the global scratch
     int swiglu;             // 1: x is [M][2K] (gate | up); the GEMV's input is silu(gate) * up
+    // Greedy argmax fused into the cluster split-K finish (nullptr: none): each
+    // CTA reduces the outputs it writes to one (value, index) candidate,
+    // amax_cand[m * kArgmaxSlots + blockIdx.x], and the CTA that takes token m's
+    // last ticket picks ids[m] and re-arms the ticket.
+    int32_t* ids;           // [M]
+    float2* amax_cand;      // [M][kArgmaxSlots]
+    unsigned* amax_tickets; // [M], zero between calls
 };
+
+// Candidate slots per token for the argmax (at least the decode grid and the
+// argmax kernel's chunk count).
+constexpr int kArgmaxSlots = 256;
+
+// Total order of the greedy pick: a NaN above every number, then the usual
+// order, and among equal values the smaller index.
+__device__ __forceinline__ bool argmax_better(float v, int i, float bv, int bi)
+{
+    const bool vn = v != v, bn = bv != bv;
+    if (vn != bn) return vn;
+    if (!vn && v != bv) return v > bv;
+    return i < bi;
+}
 
 struct PrefillParams {
     const uint32_t* bits;   // [N][K/32], prefill bit order (see repack.cu)
@@ -155,7 +178,9 @@ cudaError_t bitlin_launch_repack_prefill(const uint32_t* bits, int N, int K, uin
 cudaError_t bitlin_launch_check_signs(const float* signs, int K, int* bad, cudaStream_t s);
 cudaError_t bitlin_launch_decode(const bitlin_impl::DecodeParams& p, int num_sms, cudaStream_t s);
 // Kernels one bitlin_launch_decode of p launches: 1 (cluster split-K) or 2 (GEMV, then the sum).
-cudaError_t bitlin_decode_kernels(const bitlin_impl::DecodeParams& p, int num_sms, int* kernels);
+// *fused_argmax: 1 when that launch can also pick the argmax (p.ids), 0 otherwise.
+cudaError_t bitlin_decode_kernels(const bitlin_impl::DecodeParams& p, int num_sms, int* kernels,
+                                  int* fused_argmax = nullptr);
 cudaError_t bitlin_launch_argmax(const float* y, int M, int N, void* cand, unsigned* tickets, int32_t* ids,
                                  cudaStream_t s);
 size_t bitlin_argmax_scratch_bytes(int M);

@@ -94,6 +94,9 @@ extern "C" bitlin_status bitlin_forward_noalloc(bitlin_t h, const float* x, int 
             p.cluster = 0;
             p.allow_cluster = 0;  // this entry point's split-K goes through the static scratch
             p.swiglu = 0;
+            p.ids = nullptr;
+            p.amax_cand = nullptr;
+            p.amax_tickets = nullptr;
             e = bitlin_launch_decode(p, h->num_sms, s);
         }
     }

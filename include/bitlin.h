@@ -199,6 +199,13 @@ bitlin_status bitlin_forward_noalloc(bitlin_t h, const float* x, int M, float* y
  *           on the first call with a new largest M).
  *   ids     device pointer, int32 [M], overwritten.
  *
+ * Asynchronous on `stream`.  When the decode GEMV sums its split-K slices
+ * inside thread-block clusters (one token on the vocabulary matrix), the pick
+ * is fused into that kernel's finish: each CTA reduces the scores it writes
+ * to one candidate and the last CTA to finish picks; otherwise a second
+ * kernel reads the scores back and picks.  The first call with a new largest
+ * M allocates the candidate and ticket buffers the handle keeps (the tickets
+ * are zeroed in stream order on `stream`).
  * Errors: BITLIN_EINVAL (NULL handle/x/ids, M < 1), BITLIN_ENOMEM,
  * BITLIN_ECUDA, and the handle's sticky error.
  */

@@ -343,12 +343,16 @@ def test_auto_path_choice(hrb):
 
 def test_plan_reports_path_and_kernels(hrb):
     """bitlin_plan: the path of each M range, one kernel for the cluster split-K (10 slices at
-    K = 5120), two (GEMV + sum) for 34 slices at K = 17408, two (rotation + GEMM) on the tensor
-    paths; a forced path is reported as forced."""
+    K = 5120 in clusters of 10; 34 slices at K = 17408 in clusters of 12 CTAs of 3 slices),
+    two (GEMV + sum) beyond four slices per CTA (K = 65536), two (rotation + GEMM) on the
+    tensor paths; a forced path is reported as forced."""
     gate = make_layer(hrb, *inputs("ffn_gate", 1)[1:4], 0)
     down = make_layer(hrb, *inputs("ffn_down", 1)[1:4], 0)
     assert [gate.plan(m) for m in (1, 2, 6, 7, 63, 64)] == [(1, 1), (1, 1), (1, 1), (3, 2), (3, 2), (2, 2)]
-    assert down.plan(1) == (1, 2)
+    assert down.plan(1) == (1, 1)
+    wide = make_layer(hrb, synth.random_bits(3, 64, 65536), synth.random_scales(3, 64, 65536, 0.005, 0.03),
+                      synth.random_signs(3, 65536), 0)
+    assert wide.plan(1) == (1, 2)
     gate.set_path(1)
     assert gate.plan(200) == (1, 2)  # 200 tokens' partials do not fit shared memory: scratch + sum
 
@@ -446,6 +450,29 @@ def test_argmax_ties_take_the_smallest_index(hrb):
     assert layer.argmax(torch.from_numpy(x).cuda()).cpu().numpy()[0] == 100
     z = torch.zeros((2, w.K), dtype=torch.float32, device="cuda")
     assert layer.argmax(z).cpu().numpy().tolist() == [0, 0]
+
+
+def test_argmax_consecutive_calls_and_nan(hrb):
+    """Several calls in a row on one handle (the pick's ticket is re-armed by each call):
+    each id is the argmax of that call's scores, at one token (the pick fused into the
+    product's finish) and at two; a NaN input makes every score NaN, and a NaN counts as the
+    largest value, so the smallest index wins."""
+    N, K = 20000, 5120
+    bits = synth.random_bits(21, N, K)
+    scales = synth.random_scales(21, N, K, 0.005, 0.03)
+    signs = synth.random_signs(21, K)
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    for M in (1, 2):
+        for seed in (1, 2, 3):
+            x = torch.from_numpy(synth.random_x(seed, M, K)).cuda()
+            lg = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            ids = layer.argmax(x, logits=lg).cpu().numpy()
+            assert ids.tolist() == np.argmax(lg.cpu().numpy(), axis=1).tolist()
+    x = torch.from_numpy(synth.random_x(4, 1, K)).cuda()
+    x[0, 77] = float("nan")
+    assert layer.argmax(x).cpu().numpy().tolist() == [0]
+    torch.cuda.synchronize()
+    assert layer.get_error() == 0
 
 
 # ------------------------------------------------------------------ embedding (inverse rotation)
