@@ -76,11 +76,9 @@ struct DecodeParams {
     int M, N, K, S, T, perm;
     int ctas_per_slice;     // set by the launcher
     int split_q, split_r;   // set by the launcher: T = split_q * ctas_per_slice + split_r
+    unsigned s_mul;         // set by the launcher: ceil(2^32 / S), for division by S in the kernel
     int pbuf_bytes;         // set by the launcher: cluster split-K partial sums per CTA (bytes)
     int cluster;            // set by the launcher: 1 = split-K summed across a thread-block cluster
-    int csize;              // set by the launcher: CTAs per cluster, C = ceil(S / cspc)
-    int cspc;               // set by the launcher: slices per CTA of a cluster (rank r: r*cspc ...)
-    unsigned c_mul;         // set by the launcher: ceil(2^32 / C), for division by C in the kernel
     int allow_cluster;      // set by the caller: 0 keeps the split-K in the global scratch
     int swiglu;             // 1: x is [M][2K] (gate | up); the GEMV's input is silu(gate) * up
     // Greedy argmax fused into the cluster split-K finish (nullptr: none): each

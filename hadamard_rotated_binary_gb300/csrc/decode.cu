@@ -82,8 +82,7 @@ constexpr int kDecodeSmem = kLutBytes + kSmemTranspose + kSmemSlice;
 constexpr int kLut2Off = (kDecodeSmem + 127) & ~127;
 constexpr int kPbufOff = (kDecodeSmem + 15) & ~15;  // M = 1
 constexpr int kPbufOff2 = kLut2Off + kLutBytes;     // M >= 2
-constexpr int kMaxClusterSlices = 16;    // CTAs per cluster at most (non-portable size)
-constexpr int kMaxClusterSegments = 4;   // slices per CTA at most on the cluster path (K <= 32768)
+constexpr int kMaxClusterSlices = 16;
 // Warps of the wide one-token CTA (cluster split-K with at most 48 tiles per
 // CTA): two tiles per warp at most, a 2-deep register ring, 80 registers per
 // thread (warps are dealt round robin to the SM's four sub-partitions of
@@ -486,8 +485,8 @@ constexpr int kDecodeRegs = BITLIN_DECODE_REGS;
 // no second barrier is needed before the CTAs exit.
 // v / S as umulhi(v, ceil(2^32 / S)): exact for S in [2, 16] and v < 2^17 (the
 // partial sums of a cluster fit 96 KB, so its tile count is below 768).
-__device__ __forceinline__ int div_c(const DecodeParams& p, int v) { return (int)__umulhi((unsigned)v, p.c_mul); }
-__device__ __forceinline__ int cluster_slots(const DecodeParams& p, int ntile) { return div_c(p, ntile + p.csize - 1); }
+__device__ __forceinline__ int div_s(const DecodeParams& p, int v) { return (int)__umulhi((unsigned)v, p.s_mul); }
+__device__ __forceinline__ int cluster_slots(const DecodeParams& p, int ntile) { return div_s(p, ntile + p.S - 1); }
 
 // Best (value, index) over the CTA's threads in the argmax order; the result
 // is valid in thread 0.  red: shared scratch of 64 words, free on entry.
@@ -529,16 +528,17 @@ __device__ __forceinline__ void cta_best(float& bv, int& bi, float* red, int thr
 // (bv, bi) is this thread's best over the outputs it wrote.  The CTA's best
 // becomes candidate blockIdx.x of token m; the CTA that takes the token's last
 // ticket picks among all candidates (the order is total, so the result does
-// not depend on which CTA that is) and re-arms the ticket.
-__device__ __forceinline__ void finish_argmax(const DecodeParams& p, int m, float bv, int bi, float* red,
-                                              int threads)
+// not depend on which CTA that is) and re-arms the ticket.  Not inlined: it
+// runs once per call, and inlined it cost the lookup loop registers.
+__device__ __noinline__ void finish_argmax(int32_t* ids, float2* cand, unsigned* tickets, int m, float bv, int bi,
+                                           float* red, int threads)
 {
     cta_best(bv, bi, red, threads);
     int* last = reinterpret_cast<int*>(red + 64);
     if (threadIdx.x == 0) {
-        p.amax_cand[(size_t)m * kArgmaxSlots + blockIdx.x] = make_float2(bv, __int_as_float(bi));
+        cand[(size_t)m * kArgmaxSlots + blockIdx.x] = make_float2(bv, __int_as_float(bi));
         __threadfence();
-        *last = atomicAdd(p.amax_tickets + m, 1u) == gridDim.x - 1;
+        *last = atomicAdd(tickets + m, 1u) == gridDim.x - 1;
     }
     __syncthreads();
     if (!*last) return;
@@ -546,7 +546,7 @@ __device__ __forceinline__ void finish_argmax(const DecodeParams& p, int m, floa
     bv = -__int_as_float(0x7f800000);
     bi = 0x7fffffff;
     for (int j = (int)threadIdx.x; j < (int)gridDim.x; j += threads) {
-        const float2 c = __ldcg(p.amax_cand + (size_t)m * kArgmaxSlots + j);
+        const float2 c = __ldcg(cand + (size_t)m * kArgmaxSlots + j);
         if (argmax_better(c.x, __float_as_int(c.y), bv, bi)) {
             bv = c.x;
             bi = __float_as_int(c.y);
@@ -554,56 +554,56 @@ __device__ __forceinline__ void finish_argmax(const DecodeParams& p, int m, floa
     }
     cta_best(bv, bi, red, threads);
     if (threadIdx.x == 0) {
-        p.ids[m] = bi;
-        p.amax_tickets[m] = 0u;  // re-armed for the next call
+        ids[m] = bi;
+        tickets[m] = 0u;  // re-armed for the next call
     }
 }
 
-// red: shared scratch for the fused argmax (65 words; the transpose buffer,
-// free once the tables are built).
+// AM: the greedy argmax is fused into the finish (finish_argmax); red is its
+// shared scratch (65 words: the transpose buffer, free once the tables are built).
+template <bool AM>
 __device__ __forceinline__ void cluster_finish(const DecodeParams& p, int ta, int tb, int rank, const float* pbuf,
                                                int threads, float* red)
 {
     ptx::cluster_sync();
-    const int ntile = tb - ta, S = p.S, C = p.csize, LT = cluster_slots(p, ntile);
-    const int mine = ntile > rank ? div_c(p, ntile - rank + C - 1) : 0;  // tiles rank, rank + C, ...
+    const int ntile = tb - ta, S = p.S, LT = cluster_slots(p, ntile);
+    const int mine = ntile > rank ? div_s(p, ntile - rank + S - 1) : 0;  // tiles rank, rank + S, ...
     const int stride = LT * kTileRows;
     for (int m = 0; m < p.M; ++m) {
-        float bv = -__int_as_float(0x7f800000);  // this thread's best output (fused argmax)
+        float bv = -__int_as_float(0x7f800000);  // AM: this thread's best output
         int bi = 0x7fffffff;
         for (int i = (int)threadIdx.x; i < mine * kTileRows; i += threads) {
             const int slot = i >> 5, lane = i & 31;
             const float* src = pbuf + (m * S * LT + slot) * kTileRows + lane;
-            // Up to 16 loads in flight at once, then their sum in slice order.
-            float sum = 0.f;
-            for (int s0 = 0; s0 < S; s0 += kMaxClusterSlices) {
-                float v[kMaxClusterSlices];
+            // All S loads in flight at once, then the sum in slice order.
+            float v[kMaxClusterSlices];
 #pragma unroll
-                for (int s = 0; s < kMaxClusterSlices; ++s) {
-                    v[s] = 0.f;
-                    if (s0 + s < S) v[s] = src[(s0 + s) * stride];
-                }
-#pragma unroll
-                for (int s = 0; s < kMaxClusterSlices; ++s)
-                    if (s0 + s < S) sum += v[s];
+            for (int s = 0; s < kMaxClusterSlices; ++s) {
+                v[s] = 0.f;
+                if (s < S) v[s] = src[s * stride];
             }
-            const int n = (ta + slot * C + rank) * kTileRows + lane;
+            float sum = 0.f;
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSlices; ++s)
+                if (s < S) sum += v[s];
+            const int n = (ta + slot * S + rank) * kTileRows + lane;
             if (n < p.N) {
                 p.y[(size_t)m * p.N + n] = sum;
-                if (argmax_better(sum, n, bv, bi)) {
+                if (AM && argmax_better(sum, n, bv, bi)) {
                     bv = sum;
                     bi = n;
                 }
             }
         }
-        if (p.ids) finish_argmax(p, m, bv, bi, red, threads);
+        if (AM) finish_argmax(p.ids, p.amax_cand, p.amax_tickets, m, bv, bi, red, threads);
     }
 }
 
 // TWO: tokens are taken two at a time (M >= 2), with a 2-deep register ring so
 // that both tokens' accumulators fit the register budget; M = 1 keeps the
 // 4-deep ring.  AL (M = 1 only): the table at a 64 KB-aligned shared address.
-template <bool TWO, bool AL, int NW>
+// AM (cluster split-K only): the greedy argmax fused into the finish.
+template <bool TWO, bool AL, int NW, bool AM = false>
 __global__ void __maxnreg__(NW == kDecodeWarps ? kDecodeRegs : 80) bitlin_decode_gemv(const DecodeParams p)
 {
     static_assert(NW == kDecodeWarps || (!TWO && AL), "more warps only for one token with the aligned table");
@@ -636,19 +636,16 @@ __global__ void __maxnreg__(NW == kDecodeWarps ? kDecodeRegs : 80) bitlin_decode
     // otherwise (more slices than CTAs) the units are split evenly.
     int u0, u1;
     int s0;        // the slice of the CTA's first segment
-    int rank = 0;  // cluster mode: this CTA's rank in the cluster; its slices are rank * cspc + j
-    int nseg = 0;  // cluster mode: the CTA's slices (one segment of the cluster's tile range each)
+    int rank = 0;  // cluster mode: this CTA's slice = its rank in the cluster
     // The T tiles of a slice are split over ctas_per_slice = ncl ranges, the
     // first split_r of them one tile longer: range c starts at
     // c * split_q + min(c, split_r).  No division in the cluster case.
     if (p.cluster) {
-        // Cluster c (C consecutive blocks) covers range c of every slice; its
-        // CTA of rank r takes slices r * cspc ... (one slice each when S <= 16).
-        const int c = (int)__umulhi(blockIdx.x, p.c_mul);  // blockIdx.x / C
-        rank = (int)blockIdx.x - c * p.csize;
-        s0 = rank * p.cspc;
-        nseg = min(p.cspc, p.S - s0);
-        u0 = s0 * p.T + c * p.split_q + min(c, p.split_r);
+        // Cluster c (S consecutive blocks, one per slice) covers range c of every slice.
+        const int c = (int)__umulhi(blockIdx.x, p.s_mul);  // blockIdx.x / S
+        rank = (int)blockIdx.x - c * p.S;
+        s0 = rank;
+        u0 = rank * p.T + c * p.split_q + min(c, p.split_r);
         u1 = u0 + p.split_q + (c < p.split_r ? 1 : 0);
     } else if (p.ctas_per_slice > 0) {
         const int s = (int)blockIdx.x / p.ctas_per_slice, c = (int)blockIdx.x - s * p.ctas_per_slice;
@@ -677,15 +674,6 @@ __global__ void __maxnreg__(NW == kDecodeWarps ? kDecodeRegs : 80) bitlin_decode
         const int pu = min(u1 - u0, kPrefetchUnits);
         prefetch_l2(p.bits + (size_t)u0 * 128, (size_t)pu * 2048, threadIdx.x);
         prefetch_l2(p.scales + (size_t)u0 * 32, (size_t)pu * 256, (threadIdx.x + 128) % kDecodeThreads);
-    } else {
-        // Several slices per CTA: the later segments' weights into L2 now, so
-        // that each later segment's ring loads (issued before its transform
-        // and table build) are served from L2.
-        for (int j = 1; j < nseg; ++j) {
-            const size_t uj = (size_t)u0 + (size_t)j * p.T;
-            prefetch_l2(p.bits + uj * 128, (size_t)(u1 - u0) * 2048, threadIdx.x);
-            prefetch_l2(p.scales + uj * 32, (size_t)(u1 - u0) * 256, (threadIdx.x + 128) % kDecodeThreads);
-        }
     }
     // Before the wait: this warp's first tiles (ta + warp + NW * j, j < RING) and
     // the signs of the first segment, whose latency then overlaps the wait, and
@@ -713,21 +701,11 @@ __global__ void __maxnreg__(NW == kDecodeWarps ? kDecodeRegs : 80) bitlin_decode
     bool triggered = false;
     bool preloaded = true;  // the ring and the signs hold the first (segment, token)
 
-    for (int u = u0, seg = 0;; ++seg) {
-        int s, ta, tb;
-        if (p.cluster) {
-            // The CTA's slices s0 .. s0 + nseg - 1, each over the cluster's tile range.
-            if (seg == nseg) break;
-            s = s0 + seg;
-            ta = u0 - s0 * p.T;
-            tb = ta + (u1 - u0);
-        } else {
-            if (u >= u1) break;
-            s = u == u0 ? s0 : u / p.T;  // no division before the first segment's loads
-            ta = u - s * p.T;
-            tb = min(p.T, ta + (u1 - u));
-            u += tb - ta;
-        }
+    for (int u = u0; u < u1;) {
+        const int s = u == u0 ? s0 : u / p.T;  // no division before the first segment's loads
+        const int ta = u - s * p.T;
+        const int tb = min(p.T, ta + (u1 - u));
+        u += tb - ta;
 
         // Tokens two at a time: both tables are built, then every weight tile
         // loaded serves both tokens' lookups.
@@ -781,10 +759,10 @@ __global__ void __maxnreg__(NW == kDecodeWarps ? kDecodeRegs : 80) bitlin_decode
             auto put = [&](int mm, int t, float v) {
                 if (p.cluster) {
                     const int lt = t - ta;
-                    // lt / C as umulhi(lt, ceil(2^32 / C)): exact for C in [2, 16], lt < 2^17
+                    // lt / S as umulhi(lt, ceil(2^32 / S)): exact for S in [2, 16], lt < 2^17
                     // (the partials of a cluster fit 96 KB, so lt < 768).
-                    const int q = (int)__umulhi((unsigned)lt, p.c_mul), r = lt - q * p.csize;
-                    const uint32_t off = (uint32_t)((((mm * p.S) + s) * LT + q) * kTileRows + lane);
+                    const int q = (int)__umulhi((unsigned)lt, p.s_mul), r = lt - q * p.S;
+                    const uint32_t off = (uint32_t)((((mm * p.S) + rank) * LT + q) * kTileRows + lane);
                     ptx::st_cluster(ptx::cluster_map(pbase + 4u * off, r), v);
                 } else {
                     p.partials[((size_t)s * p.M + mm) * npad + (size_t)t * kTileRows + lane] = v;
@@ -825,10 +803,7 @@ __global__ void __maxnreg__(NW == kDecodeWarps ? kDecodeRegs : 80) bitlin_decode
                 if (!more) break;
             }
         }
-    }
-    if (p.cluster) {
-        const int ta = u0 - s0 * p.T;
-        cluster_finish(p, ta, ta + (u1 - u0), rank, pbuf, 32 * NW, tbuf);
+        if (p.cluster) cluster_finish<AM>(p, ta, tb, rank, pbuf, 32 * NW, tbuf);
     }
     if (!triggered) pdl_launch_dependents();
 }
@@ -920,7 +895,9 @@ cudaError_t configure_decode(const DecodeDevice** out)
         if (r == cudaSuccess) r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
         if (r == cudaSuccess && c.max_smem < kPbufOff2) r = cudaErrorInvalidConfiguration;
         for (auto k : {bitlin_decode_gemv<false, false, kDecodeWarps>, bitlin_decode_gemv<false, true, kDecodeWarps>,
-                       bitlin_decode_gemv<false, true, kWideWarps>, bitlin_decode_gemv<true, false, kDecodeWarps>}) {
+                       bitlin_decode_gemv<false, true, kWideWarps>, bitlin_decode_gemv<true, false, kDecodeWarps>,
+                       bitlin_decode_gemv<false, false, kDecodeWarps, true>,
+                       bitlin_decode_gemv<true, false, kDecodeWarps, true>}) {
             if (r == cudaSuccess) r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, c.max_smem);
             if (r == cudaSuccess) r = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         }
@@ -944,27 +921,22 @@ DecodeShape decode_shape(const DecodeParams& p, int num_sms, const DecodeDevice&
     DecodeShape d{0, p.M >= 2 ? kPbufOff2 : kDecodeSmem, 0, 0, 0};  // two tables from M = 2
     int pbytes = 0;  // cluster split-K partial sums per CTA
     q.cluster = 0;
-    // Split-K across a cluster of C CTAs, each taking cspc consecutive slices
-    // (C = S when S <= 16; otherwise cspc = ceil(S / 16) and C = ceil(S / cspc),
-    // so ffn_down's 34 slices go to clusters of 12), when the partial sums fit
-    // shared memory; else through the global scratch and a second kernel.
-    q.cspc = (p.S + kMaxClusterSlices - 1) / kMaxClusterSlices;
-    q.csize = (p.S + q.cspc - 1) / q.cspc;
-    q.c_mul = 0xFFFFFFFFu / (unsigned)q.csize + 1u;  // ceil(2^32 / C); C >= 2 since S = K / 512 >= 2
-    if (p.allow_cluster && q.cspc <= kMaxClusterSegments) {
-        const int C = q.csize;
-        const int maxc = dc.max_clusters[C];
+    q.s_mul = 0xFFFFFFFFu / (unsigned)p.S + 1u;  // ceil(2^32 / S); S = K / 512 >= 2
+    // Split-K across a cluster when the slices fit one (S <= 16) and the
+    // partial sums fit shared memory; else through the global scratch.
+    if (p.allow_cluster && p.S <= kMaxClusterSlices) {
+        const int maxc = dc.max_clusters[p.S];
         if (maxc > 0) {
             const int ncl = maxc < p.T ? maxc : p.T;
-            const int lt = ((p.T + ncl - 1) / ncl + C - 1) / C;  // slots per CTA
+            const int lt = ((p.T + ncl - 1) / ncl + p.S - 1) / p.S;  // slots per CTA
             const long long pb = (long long)p.M * p.S * lt * kTileRows * 4;
             const int poff = p.M >= 2 ? kPbufOff2 : kPbufOff;
             if (pb <= kPbufBytes && poff + pb <= dc.max_smem) {
                 q.cluster = 1;
                 q.ctas_per_slice = ncl;
-                d.grid = C * ncl;
+                d.grid = p.S * ncl;
                 d.smem = poff + (int)pb;
-                d.cluster = C;
+                d.cluster = p.S;
                 pbytes = (int)pb;
             }
         }
@@ -984,7 +956,8 @@ DecodeShape decode_shape(const DecodeParams& p, int num_sms, const DecodeDevice&
         q.split_r = p.T - q.split_q * q.ctas_per_slice;
     }
     // The argmax is fused into the cluster finish when every CTA has a
-    // candidate slot; otherwise the caller runs the separate argmax kernel.
+    // candidate slot (the plain-table instances carry it); otherwise the
+    // caller runs the separate argmax kernel.
     if (!q.cluster || d.grid > kArgmaxSlots) {
         q.ids = nullptr;
         q.amax_cand = nullptr;
@@ -993,14 +966,13 @@ DecodeShape decode_shape(const DecodeParams& p, int num_sms, const DecodeDevice&
     // One token: the aligned table when the partial sums are small (the
     // allocation covers the worst-case pad below the table).
     q.pbuf_bytes = pbytes;
-    if (p.M == 1 && pbytes <= kAlMaxPbuf && kAlSmemBase + pbytes <= dc.max_smem) {
+    if (p.M == 1 && !q.ids && pbytes <= kAlMaxPbuf && kAlSmemBase + pbytes <= dc.max_smem) {
         d.aligned = 1;
         d.smem = kAlSmemBase + pbytes;
         // Cluster split-K with at most two tiles per warp of the wide CTA (every
         // tile in its ring): ffn_gate 5.64 -> 5.57 us.  The scratch path measured
         // slower with it (ffn_down 7.99 against 8.22 us), so it keeps 16 warps.
-        // With several slices per CTA the tile range is short, so 16 warps cover it.
-        if (q.cluster && q.cspc == 1 && q.split_q + (q.split_r > 0 ? 1 : 0) <= 2 * kWideWarps) d.wide = 1;
+        if (q.cluster && q.split_q + (q.split_r > 0 ? 1 : 0) <= 2 * kWideWarps) d.wide = 1;
     }
     return d;
 }
@@ -1042,7 +1014,9 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = cluster ? 2 : 1;
-    e = p.M >= 2   ? cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<true, false, kDecodeWarps>, q)
+    e = q.ids      ? (p.M >= 2 ? cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<true, false, kDecodeWarps, true>, q)
+                                : cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<false, false, kDecodeWarps, true>, q))
+        : p.M >= 2 ? cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<true, false, kDecodeWarps>, q)
         : d.wide    ? cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<false, true, kWideWarps>, q)
         : d.aligned ? cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<false, true, kDecodeWarps>, q)
                     : cudaLaunchKernelEx(&cfg, bitlin_decode_gemv<false, false, kDecodeWarps>, q);

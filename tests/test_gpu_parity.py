@@ -343,13 +343,12 @@ def test_auto_path_choice(hrb):
 
 def test_plan_reports_path_and_kernels(hrb):
     """bitlin_plan: the path of each M range, one kernel for the cluster split-K (10 slices at
-    K = 5120 in clusters of 10; 34 slices at K = 17408 in clusters of 12 CTAs of 3 slices),
-    two (GEMV + sum) beyond four slices per CTA (K = 65536), two (rotation + GEMM) on the
-    tensor paths; a forced path is reported as forced."""
+    K = 5120), two (GEMV + sum) for 34 slices at K = 17408 and for 128 at K = 65536, two
+    (rotation + GEMM) on the tensor paths; a forced path is reported as forced."""
     gate = make_layer(hrb, *inputs("ffn_gate", 1)[1:4], 0)
     down = make_layer(hrb, *inputs("ffn_down", 1)[1:4], 0)
     assert [gate.plan(m) for m in (1, 2, 6, 7, 63, 64)] == [(1, 1), (1, 1), (1, 1), (3, 2), (3, 2), (2, 2)]
-    assert down.plan(1) == (1, 1)
+    assert down.plan(1) == (1, 2)
     wide = make_layer(hrb, synth.random_bits(3, 64, 65536), synth.random_scales(3, 64, 65536, 0.005, 0.03),
                       synth.random_signs(3, 65536), 0)
     assert wide.plan(1) == (1, 2)
