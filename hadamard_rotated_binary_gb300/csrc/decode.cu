@@ -559,11 +559,13 @@ __device__ __noinline__ void finish_argmax(int32_t* ids, float2* cand, unsigned*
     }
 }
 
-// AM: the greedy argmax is fused into the finish (finish_argmax); red is its
-// shared scratch (65 words: the transpose buffer, free once the tables are built).
+// AM: the greedy argmax is fused into the finish (finish_argmax), with the
+// transpose buffer of the plain-table layout (free once the tables are built)
+// as its shared scratch; it is addressed here, not kept live from the
+// prologue, so the lookup loop keeps its registers.
 template <bool AM>
 __device__ __forceinline__ void cluster_finish(const DecodeParams& p, int ta, int tb, int rank, const float* pbuf,
-                                               int threads, float* red)
+                                               int threads)
 {
     ptx::cluster_sync();
     const int ntile = tb - ta, S = p.S, LT = cluster_slots(p, ntile);
@@ -595,7 +597,11 @@ __device__ __forceinline__ void cluster_finish(const DecodeParams& p, int ta, in
                 }
             }
         }
-        if (AM) finish_argmax(p.ids, p.amax_cand, p.amax_tickets, m, bv, bi, red, threads);
+        if (AM) {
+            extern __shared__ __align__(128) unsigned char smem[];
+            finish_argmax(p.ids, p.amax_cand, p.amax_tickets, m, bv, bi,
+                          reinterpret_cast<float*>(smem + kLutBytes), threads);
+        }
     }
 }
 
@@ -606,6 +612,7 @@ __device__ __forceinline__ void cluster_finish(const DecodeParams& p, int ta, in
 template <bool TWO, bool AL, int NW, bool AM = false>
 __global__ void __maxnreg__(NW == kDecodeWarps ? kDecodeRegs : 80) bitlin_decode_gemv(const DecodeParams p)
 {
+    static_assert(!(AM && AL), "the fused argmax uses the plain-table layout");
     static_assert(NW == kDecodeWarps || (!TWO && AL), "more warps only for one token with the aligned table");
     static_assert(!(TWO && AL), "the aligned table is for one token at a time");
     constexpr int RING = TWO || NW != kDecodeWarps ? 2 : kRing;
@@ -803,7 +810,14 @@ __global__ void __maxnreg__(NW == kDecodeWarps ? kDecodeRegs : 80) bitlin_decode
                 if (!more) break;
             }
         }
-        if (p.cluster) cluster_finish<AM>(p, ta, tb, rank, pbuf, 32 * NW, tbuf);
+        if (!AM && p.cluster) cluster_finish<false>(p, ta, tb, rank, pbuf, 32 * NW);
+    }
+    // The fused-argmax instance finishes after the loop, from the CTA's unit
+    // range (one segment on the cluster path): with the finish inside the
+    // loop it needed more than 128 registers.
+    if (AM && p.cluster) {
+        const int ta = u0 - s0 * p.T;
+        cluster_finish<true>(p, ta, ta + (u1 - u0), rank, pbuf, 32 * NW);
     }
     if (!triggered) pdl_launch_dependents();
 }
