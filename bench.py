@@ -129,15 +129,17 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def traffic_record(kernel: str, workload: str):
-    """Per-launch DRAM bytes from a committed ncu summary, if it still matches the kernel source."""
+def traffic_record(kernel: str, workload: str, M: int | None = None):
+    """Per-launch DRAM bytes from a committed ncu summary, if it still matches the kernel source.
+    A record taken at this token count ("kernel:workload:M") is preferred to one for the
+    workload at any token count ("kernel:workload")."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    entry = rec.get(f"{kernel}:{workload}")
+    entry = (rec.get(f"{kernel}:{workload}:{M}") if M is not None else None) or rec.get(f"{kernel}:{workload}")
     if not entry:
         return None
     src = os.path.join(ROOT, "hadamard_rotated_binary_gb300", "csrc", entry["source"])
@@ -176,14 +178,14 @@ def roofline(w: synth.Workload, s_per_step: float, peaks: dict, peak_kind: str, 
         achieved = w.algorithmic_bytes() / s_per_step / 1e9
         return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_kind": peak_kind, "kernel": kernel,
-                "bytes_per_launch": w.algorithmic_bytes(), "traffic": traffic_record(kernel, w.name)}
+                "bytes_per_launch": w.algorithmic_bytes(), "traffic": traffic_record(kernel, w.name, w.M)}
     kernel = "bitlin_tc_gemm"
     digits = 3 if path == 3 else 1
     flops = 2.0 * w.M * digits * w.N * w.K
     achieved = flops / s_per_step / 1e12
     return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": achieved / peaks["bf16_tflops"], "peak_kind": peak_kind, "kernel": kernel,
-            "flops_per_launch": flops, "traffic": traffic_record(kernel, w.name)}
+            "flops_per_launch": flops, "traffic": traffic_record(kernel, w.name, w.M)}
 
 
 def cpu_model() -> str:
@@ -512,7 +514,8 @@ def run_op(args, ws, rank, local, pg):
             flops = 2.0 * M * digits * N * K
             roof = {"bound": "tensor", "achieved": flops / s_step / 1e12, "peak": peaks["bf16_tflops"],
                     "unit": "TFLOP/s", "kernel": "bitlin_tc_gemm + bitlin_argmax_rows", "flops_per_launch": flops}
-        roof.update({"frac": roof["achieved"] / roof["peak"], "peak_kind": peak_kind, "traffic": None})
+        roof.update({"frac": roof["achieved"] / roof["peak"], "peak_kind": peak_kind,
+                     "traffic": traffic_record(roof["kernel"], "lm_head", M)})
         metric, config = LMHEAD_METRIC, {"workload": "lm_head", "M": M, "N": N, "K": K, "weight_copies": R,
                                          "weight_set_bytes": R * wbytes,
                                          "l2": f"inputs larger than L2: {R} distinct copies cycled"}

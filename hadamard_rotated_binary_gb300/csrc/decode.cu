@@ -824,12 +824,22 @@ __global__ void __maxnreg__(NW == kDecodeWarps ? kDecodeRegs : 80) bitlin_decode
 
 // Split-K outside a cluster: the sum of the GEMV's partials [S][M][T*32].
 // Thread i owns output (m, n) = (i / N, i % N) and adds its S partials in
-// slice order s = 0..S-1 (the order of the cluster path), 16 loads in flight.
+// slice order s = 0..S-1 (the order of the cluster path), with up to B loads
+// in flight: B = 48 when S > 16 (one round at K = 17408: ffn_down 8.0 -> 7.2 us
+// per call against rounds of 16), else 16 (48 registers; the wide variant's 96
+// halve the occupancy, and the vocabulary matrix at M = 4, almost a million
+// outputs, measured 134 against 118 us per call with it).
+// The grid stays small on purpose (one output per thread): the next call's
+// GEMV, launched early, needs whole SMs, and it finds them on the SMs this
+// grid leaves free (160 CTAs of 32 outputs measured 10.8 against 8.0 us per
+// ffn_down call).
 constexpr int kReduceThreads = 128;
+template <int B>
 __global__ void __launch_bounds__(kReduceThreads)
     bitlin_decode_reduce(const float* __restrict__ partials, float* __restrict__ y, int M, int N, int S,
                          long long npad)
 {
+    constexpr int kReduceBatch = B;
     // The successor may launch at once: it reads nothing this kernel writes
     // before its own wait, which covers this whole grid.
     pdl_launch_dependents();
@@ -840,13 +850,13 @@ __global__ void __launch_bounds__(kReduceThreads)
     const float* src = partials + (size_t)m * npad + n;
     const size_t step = (size_t)M * npad;
     float sum = 0.f;
-    for (int s0 = 0; s0 < S; s0 += 16) {
-        const int cnt = min(16, S - s0);
-        float v[16];
+    for (int s0 = 0; s0 < S; s0 += kReduceBatch) {
+        const int cnt = min(kReduceBatch, S - s0);
+        float v[kReduceBatch];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = j < cnt ? __ldcg(src + (size_t)(s0 + j) * step) : 0.f;
+        for (int j = 0; j < kReduceBatch; ++j) v[j] = j < cnt ? __ldcg(src + (size_t)(s0 + j) * step) : 0.f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
+        for (int j = 0; j < kReduceBatch; ++j)
             if (j < cnt) sum += v[j];
     }
     y[(size_t)m * N + n] = sum;
@@ -1043,6 +1053,6 @@ cudaError_t bitlin_launch_decode(const DecodeParams& p, int num_sms, cudaStream_
     rc.stream = s;
     rc.attrs = attr;
     rc.numAttrs = 1;
-    return cudaLaunchKernelEx(&rc, bitlin_decode_reduce, static_cast<const float*>(p.partials), p.y, p.M, p.N,
-                              p.S, (long long)p.T * kTileRows);
+    return cudaLaunchKernelEx(&rc, p.S > 16 ? bitlin_decode_reduce<48> : bitlin_decode_reduce<16>,
+                              static_cast<const float*>(p.partials), p.y, p.M, p.N, p.S, (long long)p.T * kTileRows);
 }

@@ -39,6 +39,22 @@ def test_traffic_reported_only_for_the_captured_source(tmp_path, monkeypatch):
     assert bench.traffic_record("bitlin_tc_gemm", "prefill") is None
 
 
+def test_traffic_prefers_the_record_at_the_same_token_count(tmp_path, monkeypatch):
+    csrc = tmp_path / "hadamard_rotated_binary_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    src = b"// kernel as profiled\n"
+    (csrc / "decode.cu").write_bytes(src)
+    (tmp_path / "profiles").mkdir()
+    digest = hashlib.sha256(src).hexdigest()
+    rec = {"bitlin_decode_gemv:gate_up:4": {"bytes_per_launch": 25_225_472, "source": "decode.cu", "sha256": digest},
+           "bitlin_decode_gemv:gate_up": {"bytes_per_launch": 25_200_000, "source": "decode.cu", "sha256": digest}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_record("bitlin_decode_gemv", "gate_up", 4) == 25_225_472
+    assert bench.traffic_record("bitlin_decode_gemv", "gate_up", 1) == 25_200_000
+    assert bench.traffic_record("bitlin_decode_gemv", "gate_up") == 25_200_000
+
+
 def test_traffic_is_null_once_the_source_changed(tmp_path, monkeypatch):
     _fake_tree(tmp_path, b"// kernel as it is now\n", b"// kernel as profiled\n", 12_615_509)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
@@ -52,7 +68,7 @@ def test_traffic_is_null_without_a_record(tmp_path, monkeypatch):
 
 
 def test_decode_roofline_is_algorithmic_bytes_over_step_time(monkeypatch):
-    monkeypatch.setattr(bench, "traffic_record", lambda kernel, workload: None)
+    monkeypatch.setattr(bench, "traffic_record", lambda kernel, workload, M=None: None)
     w = synth.workload("ffn_gate")
     s_per_step = 5.7e-6
     r = bench.roofline(w, s_per_step, PEAKS, "measured", path=1, kernels=1)
@@ -67,7 +83,7 @@ def test_decode_roofline_is_algorithmic_bytes_over_step_time(monkeypatch):
 
 @pytest.mark.parametrize("path,digits", [(2, 1), (3, 3)])
 def test_tensor_roofline_counts_digit_columns(monkeypatch, path, digits):
-    monkeypatch.setattr(bench, "traffic_record", lambda kernel, workload: None)
+    monkeypatch.setattr(bench, "traffic_record", lambda kernel, workload, M=None: None)
     w = synth.workload("gate_up", 16)
     s_per_step = 38.3e-6
     r = bench.roofline(w, s_per_step, PEAKS, "measured", path=path, kernels=2)
