@@ -3,9 +3,10 @@
 Every case draws its inputs from the seeded generator, runs the library on
 cuda:0, and compares with the oracle's f64 evaluation of the same inputs:
 max relative L2 error per token row <= 1e-5 on the decode path and <= 1e-2
-on the tensor-core path.  Full-size cases compare every output where the
-oracle finishes in seconds, else a seeded sample of rows (always including
-the first and last).
+on the tensor-core path.  Full-size cases of the five workloads compare every
+output (the prefill case takes the OpenMP oracle some seconds); the other
+shapes and the largest widths compare a seeded sample of rows (always
+including the first and last).
 """
 import os
 
@@ -97,12 +98,12 @@ def test_ssm_out_permutation_matters(hrb):
 
 @pytest.mark.parametrize("M", [1, 4, 16])
 def test_gate_up_decode_sweep(hrb, M):
+    """Config 4 below M = 64, every output: the decode GEMV at M = 1 and 4 (two tokens per
+    pass), the exact three-digit tensor path at M = 16."""
     w, bits, scales, signs, x = inputs("gate_up", M)
     y = run(make_layer(hrb, bits, scales, signs, w.perm), x)
-    rows = None if M == 1 else synth.sample_rows(w.seed, w.N, 1536)
-    ref = oracle.forward(bits, scales, signs, w.perm, x, rows)
-    got = y if rows is None else y[:, rows]
-    assert max_rel_l2(got, ref) <= DECODE_TOL
+    ref = oracle.forward(bits, scales, signs, w.perm, x)
+    assert max_rel_l2(y, ref) <= DECODE_TOL
 
 
 @pytest.mark.parametrize("name,M", [("attn_qkv", 4), ("attn_gate", 16), ("attn_q", 8), ("attn_kv", 3),
@@ -117,31 +118,34 @@ def test_attention_shapes_small_batch(hrb, name, M):
 
 
 def test_gate_up_m64_both_paths(hrb):
+    """Config 4 at M = 64, every output: the bf16 tensor path (the automatic choice) within
+    1e-2 and the decode GEMV (forced) within 1e-5."""
     w, bits, scales, signs, x = inputs("gate_up", 64)
     layer = make_layer(hrb, bits, scales, signs, w.perm)
-    rows = synth.sample_rows(w.seed, w.N, 1024)
-    ref = oracle.forward(bits, scales, signs, w.perm, x, rows)
+    ref = oracle.forward(bits, scales, signs, w.perm, x)
     y_auto = run(layer, x)  # M = 64 selects the tensor-core path
-    assert max_rel_l2(y_auto[:, rows], ref) <= PREFILL_TOL
+    assert max_rel_l2(y_auto, ref) <= PREFILL_TOL
     y_dec = run(layer, x, path=hrb.PATH_DECODE)
-    assert max_rel_l2(y_dec[:, rows], ref) <= DECODE_TOL
+    assert max_rel_l2(y_dec, ref) <= DECODE_TOL
 
 
 # ------------------------------------------------------------------ prefill
 
-def test_prefill_full_size_sampled_rows(hrb):
+def test_prefill_full_size_every_output(hrb):
+    """Config 5 (1024 tokens through the 17,408 x 5,120 matrix), every output against the
+    oracle within 1e-2."""
     w, bits, scales, signs, x = inputs("prefill")
     y = run(make_layer(hrb, bits, scales, signs, w.perm), x)
-    rows = synth.sample_rows(w.seed, w.N, 160)
-    ref = oracle.forward(bits, scales, signs, w.perm, x, rows)
-    assert max_rel_l2(y[:, rows], ref) <= PREFILL_TOL
+    assert np.all(np.isfinite(y))
+    ref = oracle.forward(bits, scales, signs, w.perm, x)
+    assert max_rel_l2(y, ref) <= PREFILL_TOL
     # Against the oracle with bf16-rounded activations what remains is the f32
     # accumulation and the few elements whose rounding to bf16 flips because
     # the kernel rounds its f32 value and the oracle its f64 value (one bf16
-    # ulp, 2^-8 relative, each): well under 1e-3.
+    # ulp, 2^-8 relative, each): well under 1e-3.  A seeded sample of rows.
+    rows = synth.sample_rows(w.seed, w.N, 1024)
     ref16 = oracle.forward(bits, scales, signs, w.perm, x, rows, round_bf16=True)
     assert max_rel_l2(y[:, rows], ref16) <= BF16_DIAG_TOL
-    assert np.all(np.isfinite(y))
 
 
 @pytest.mark.parametrize("N,K,M,perm", [(300, 2048, 65, 0), (129, 1024, 130, 0), (256, 6144, 128, 1),
