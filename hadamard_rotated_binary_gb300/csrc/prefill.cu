@@ -60,24 +60,33 @@ constexpr int kBitsWarp = 14;
 constexpr int kBitsBytes = 2048;    // one group's bits: 128 rows x 4 words
 constexpr int kBitsStages = 8;      // bits run this many groups ahead of the expansion
 constexpr int kACols = 64;          // one A stage: 128 lanes x 64 columns (128 bf16 per row)
-constexpr int kTmemCols = 512;      // the whole tensor memory (one CTA per SM)
+constexpr int kTmemColsSM = 512;    // the SM's tensor memory (split between the CTAs an SM holds)
 constexpr int kMaxSplits = 8;       // split-K clusters along grid.z (portable cluster size)
 
-template <int BN>
+// OCC: CTAs per SM.  1: the whole tensor memory and about 200 KB of shared
+// memory per CTA.  2 (64-column B tiles of the exact mode): half of each (two
+// accumulator buffers and two A stages in 256 columns, five B stages, 64
+// registers a thread), so that two CTAs overlap their per-group hand-offs on
+// one SM: gate_up at M = 8 and 16 38.0 -> 33.0 us, attn_qkv at M = 16 (80
+// tiles, split-K x3 at two per SM) 20.3 -> 19.3.  Used only where the tiles
+// fill at least half of the SMs at one CTA per SM: below that (ffn_down at
+// M = 16, 40 tiles) the doubled split count measured 32.1 against 25.9 us.
+template <int BN, int OCC = 1>
 struct Cfg {
+    static constexpr int kTmemCols = kTmemColsSM / OCC;
     static constexpr int kBBytes = BN * 256;  // B tile: BN rows x 128 bf16
-    static constexpr int kSmemBudget = 200 * 1024 - kBitsStages * kBitsBytes;
+    static constexpr int kSmemBudget = (OCC == 1 ? 200 : 96) * 1024 - kBitsStages * kBitsBytes;
     static constexpr int kStagesB = kSmemBudget / kBBytes > 8 ? 8 : kSmemBudget / kBBytes;
     static constexpr int kStagesA = (kTmemCols - 2 * BN) / kACols > 6 ? 6 : (kTmemCols - 2 * BN) / kACols;
     static constexpr int kRing = kStagesA > kStagesB ? kStagesA : kStagesB;  // "done" barriers
     static_assert(kStagesB >= 3 && kStagesA >= 2, "pipeline depth");
 };
 
-template <int BN>
+template <int BN, int OCC>
 struct __align__(8) Barriers {
-    uint64_t fullB[Cfg<BN>::kStagesB];  // B tile landed (1 arrival + bytes)
-    uint64_t fullA[Cfg<BN>::kStagesA];  // A stage written (128 arrivals: one thread per row)
-    uint64_t done[Cfg<BN>::kRing];      // the MMAs of group g (index g % kRing) completed
+    uint64_t fullB[Cfg<BN, OCC>::kStagesB];  // B tile landed (1 arrival + bytes)
+    uint64_t fullA[Cfg<BN, OCC>::kStagesA];  // A stage written (128 arrivals: one thread per row)
+    uint64_t done[Cfg<BN, OCC>::kRing];      // the MMAs of group g (index g % kRing) completed
     uint64_t fullBits[kBitsStages];
     uint64_t emptyBits[kBitsStages];
     uint64_t tfull[2];
@@ -88,10 +97,11 @@ struct __align__(8) Barriers {
     int abort;
 };
 
-template <int BN>
+template <int BN, int OCC>
 constexpr int smem_bytes()
 {
-    return Cfg<BN>::kStagesB * Cfg<BN>::kBBytes + kBitsStages * kBitsBytes + (int)sizeof(Barriers<BN>) + 1024;
+    return Cfg<BN, OCC>::kStagesB * Cfg<BN, OCC>::kBBytes + kBitsStages * kBitsBytes +
+           (int)sizeof(Barriers<BN, OCC>) + 1024;
 }
 
 // Wait until the MMAs of group h have completed (h >= 0), through the "done"
@@ -103,12 +113,13 @@ __device__ __forceinline__ bool wait_done(uint64_t* done, int h, volatile int* a
     return ptx::mbar_wait_bounded(&done[h % R], (uint32_t)(h / R) & 1u, abort, budget);
 }
 
-template <int BN, bool EXACT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, bool EXACT, int OCC>
+__global__ void __launch_bounds__(kThreads, OCC)
     bitlin_tc_gemm(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_bits,
                    const PrefillParams p, int stall_test)
 {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, OCC>;
+    constexpr int kTmemCols = C::kTmemCols;
     constexpr int SB = C::kStagesB, SA = C::kStagesA, R = C::kRing;
     constexpr int kBBytes = C::kBBytes;
     constexpr int kHalf = BN / 2;                    // columns per epilogue warp
@@ -121,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     unsigned char* tileB = smem;                         // [stage][BN * 256 B]
     unsigned char* tileBits = tileB + SB * kBBytes;      // [bits stage][2 KB]: [row][4 words]
-    auto* bar = reinterpret_cast<Barriers<BN>*>(tileBits + kBitsStages * kBitsBytes);
+    auto* bar = reinterpret_cast<Barriers<BN, OCC>*>(tileBits + kBitsStages * kBitsBytes);
     volatile int* abort = &bar->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -392,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && bar->abort) atomicExch(p.dev_error, kDevErrTimeout);
 }
 
-template <int BN, bool EXACT>
+template <int BN, bool EXACT, int OCC = 1>
 cudaError_t launch(const PrefillParams& p, const void* tmap, const void* tmap_bits, int stall_test,
                    cudaStream_t s)
 {
@@ -400,8 +411,8 @@ cudaError_t launch(const PrefillParams& p, const void* tmap, const void* tmap_bi
     static PerDeviceOnce once;
     int dev = 0;
     cudaError_t ce = once.run(&dev, [](int) {
-        return cudaFuncSetAttribute(bitlin_tc_gemm<BN, EXACT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    smem_bytes<BN>());
+        return cudaFuncSetAttribute(bitlin_tc_gemm<BN, EXACT, OCC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    smem_bytes<BN, OCC>());
     });
     if (ce != cudaSuccess) return ce;
     const int rows_b = EXACT ? 4 * p.M : p.M;
@@ -411,8 +422,8 @@ cudaError_t launch(const PrefillParams& p, const void* tmap, const void* tmap_bi
     // still fit one wave, at most 8 and at least 8 K-groups each.
     int splits = 1;
     const int tiles = gx * gy, Gall = p.K / 128;
-    if (2 * tiles < p.num_sms) {
-        splits = p.num_sms / tiles;
+    if (2 * tiles < OCC * p.num_sms) {
+        splits = OCC * p.num_sms / tiles;
         if (splits > kMaxSplits) splits = kMaxSplits;
         if (splits > Gall / 8) splits = Gall / 8;
         if (splits < 1) splits = 1;
@@ -429,11 +440,11 @@ cudaError_t launch(const PrefillParams& p, const void* tmap, const void* tmap_bi
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(gx, gy, splits);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_bytes<BN>();
+    cfg.dynamicSmemBytes = smem_bytes<BN, OCC>();
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = splits > 1 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, bitlin_tc_gemm<BN, EXACT>, tb, tbits, p, stall_test);
+    return cudaLaunchKernelEx(&cfg, bitlin_tc_gemm<BN, EXACT, OCC>, tb, tbits, p, stall_test);
 }
 
 }  // namespace
@@ -453,6 +464,12 @@ cudaError_t bitlin_launch_prefill(const PrefillParams& p, const void* tmap, cons
 cudaError_t bitlin_launch_tc_exact(const PrefillParams& p, const void* tmap, const void* tmap_bits,
                                    int stall_test, cudaStream_t s)
 {
-    if (bitlin_tc_tile_width(p.M, 1) == 64) return launch<64, true>(p, tmap, tmap_bits, stall_test, s);
+    if (bitlin_tc_tile_width(p.M, 1) == 64) {
+        // Two CTAs per SM when the tiles fill at least half of the SMs at one
+        // CTA per SM (see Cfg).
+        const int tiles = (p.N + kPrefillRows - 1) / kPrefillRows;
+        if (2 * tiles >= p.num_sms) return launch<64, true, 2>(p, tmap, tmap_bits, stall_test, s);
+        return launch<64, true>(p, tmap, tmap_bits, stall_test, s);
+    }
     return launch<128, true>(p, tmap, tmap_bits, stall_test, s);
 }
