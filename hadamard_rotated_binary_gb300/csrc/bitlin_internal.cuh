@@ -112,6 +112,7 @@ struct PrefillParams {
     int M, N, K;
     int num_sms;            // for the split-K choice
     long long wait_budget_ns;
+    int tiles_x, tiles;     // set by the launcher (persistent grid): tiles along N, tiles in all
 };
 
 }  // namespace bitlin_impl
