@@ -12,10 +12,14 @@
 // registers works if each bit's butterflies pair the right values.  Vector
 // variant (x 16-byte aligned): element i = 128 p + 4 q + j (p < 8, j < 4)
 // sits in register 4p + j of lane q, so each lane reads 8 float4 and writes 8
-// groups of 4 bf16; bits 0-1 (j) and 7-9 (p) are butterflies across registers,
-// bits 2-6 (q) across lanes (warp shuffles).  Scalar variant (any alignment):
-// element i = 32 p + q in register p of lane q.  Memory-bound: 4 bytes read and
-// 2 written per element (4 x 2 in the exact mode).
+// groups of 4 bf16.  Its five register bits are element bits 0-1 and 7-9; a
+// padded shared-memory transpose puts element bits 2-6 in the registers for
+// the other five stages and a second one restores the placement for the
+// packed stores: no warp shuffles.  Scalar variant (any alignment): element
+// i = 32 p + q in register p of lane q, the stages in the same bit order (so
+// both variants round alike), lane bits by shuffles.  Memory-bound: 4 bytes
+// read and 2 written per element (4 x 2 in the exact mode).  Five CTAs of 8
+// warps per SM, so that one wave covers 1024 tokens of 5120.
 #include <cuda_bf16.h>
 
 #include "bitlin_internal.cuh"
@@ -86,6 +90,35 @@ __device__ __forceinline__ void store_rotated_vec(const float (&v)[32], __nv_bfl
     }
 }
 
+// Butterflies over the register-index bits st = lo, 2 lo, .. < hi.
+__device__ __forceinline__ void reg_butterflies(float (&v)[32], int lo, int hi)
+{
+#pragma unroll
+    for (int st = lo; st < hi; st <<= 1) {
+#pragma unroll
+        for (int p = 0; p < 32; ++p) {
+            if ((p & st) == 0) {
+                const float a = v[p], c = v[p + st];
+                v[p] = a + c;
+                v[p + st] = a - c;
+            }
+        }
+    }
+}
+
+// Butterflies over the lane bits st = lo, 2 lo, .. < hi (warp shuffles).
+__device__ __forceinline__ void lane_butterflies(float (&v)[32], int lane, int lo, int hi)
+{
+#pragma unroll
+    for (int st = lo; st < hi; st <<= 1) {
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            const float o = __shfl_xor_sync(0xffffffffu, v[r], st);
+            v[r] = (lane & st) ? (o - v[r]) : (v[r] + o);
+        }
+    }
+}
+
 __device__ __forceinline__ float silu_times(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
 // VEC: element i = 128 p + 4 q + j in register 4p + j of lane q (x 16-byte
@@ -93,7 +126,7 @@ __device__ __forceinline__ float silu_times(float g, float u) { return g / (1.f 
 // [M][2K] gate | up and the input is silu(gate) * up, SiLU(g) = g / (1 + e^-g)
 // in f32 ("Inside the One-Bit Engine", MLP station).
 template <bool VEC, bool SWIGLU>
-__global__ void __launch_bounds__(256) bitlin_rotate_bf16(const float* __restrict__ x,
+__global__ void __launch_bounds__(256, 5) bitlin_rotate_bf16(const float* __restrict__ x,
                                                           const float* __restrict__ signs, int M, int K,
                                                           int perm, int digits, __nv_bfloat16* __restrict__ xt)
 {
@@ -102,6 +135,7 @@ __global__ void __launch_bounds__(256) bitlin_rotate_bf16(const float* __restric
     // it before reading.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ float tr[VEC ? 8 : 1][32][33];
     const int lane = threadIdx.x & 31;
     const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int B = K / 1024;
@@ -126,18 +160,26 @@ __global__ void __launch_bounds__(256) bitlin_rotate_bf16(const float* __restric
             v[4 * p + 2] = a.z * sg.z;
             v[4 * p + 3] = a.w * sg.w;
         }
-        // bits 0-1: registers 4p + j, j = 0..3
+        // All five register bits (element bits 0-1 and 7-9) in registers,
+        // a transpose through shared memory, the five lane bits (element
+        // bits 2-6) in registers, and the transpose back for packed stores.
+        reg_butterflies(v, 1, 32);
+        float(*t)[33] = tr[threadIdx.x >> 5];
 #pragma unroll
-        for (int st = 1; st < 4; st <<= 1) {
+        for (int r = 0; r < 32; ++r) t[lane][r] = v[r];
+        __syncwarp();
 #pragma unroll
-            for (int r = 0; r < 32; ++r) {
-                if ((r & st) == 0) {
-                    const float a = v[r], c = v[r + st];
-                    v[r] = a + c;
-                    v[r + st] = a - c;
-                }
-            }
-        }
+        for (int r = 0; r < 32; ++r) v[r] = t[r][lane];
+        reg_butterflies(v, 1, 32);
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 32; ++r) t[r][lane] = v[r];
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 32; ++r) v[r] = t[lane][r];
+        __nv_bfloat16* out = xt + (size_t)(digits ? 4 * m : m) * K + (size_t)b * 1024;
+        store_rotated_vec(v, out, K, digits, lane);
+        return;
     } else {
 #pragma unroll
         for (int p = 0; p < 32; ++p) {
@@ -148,34 +190,16 @@ __global__ void __launch_bounds__(256) bitlin_rotate_bf16(const float* __restric
             v[p] = a * __ldg(signs + k);
         }
     }
-    // The lane bits (VEC: element bits 2-6; scalar: bits 0-4): butterflies
-    // across lanes.  The lane with the bit clear holds the low element.
-#pragma unroll
-    for (int st = 1; st < 32; st <<= 1) {
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const float o = __shfl_xor_sync(0xffffffffu, v[r], st);
-            v[r] = (lane & st) ? (o - v[r]) : (v[r] + o);
-        }
-    }
-    // The remaining bits across registers (VEC: register bits 2-4, element
-    // bits 7-9; scalar: register bits 0-4, element bits 5-9).
-#pragma unroll
-    for (int st = VEC ? 4 : 1; st < 32; st <<= 1) {
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            if ((r & st) == 0) {
-                const float a = v[r], c = v[r + st];
-                v[r] = a + c;
-                v[r + st] = a - c;
-            }
-        }
-    }
+    // Scalar placement (element 32 p + q in register p of lane q), the stages
+    // in the vector placement's order, so that both give the same roundings:
+    // element bits 0-1 across lanes, 7-9 across registers, 2-4 across lanes,
+    // 5-6 across registers.  The lane with the bit clear holds the low element.
+    lane_butterflies(v, lane, 1, 4);
+    reg_butterflies(v, 4, 32);
+    lane_butterflies(v, lane, 4, 32);
+    reg_butterflies(v, 1, 4);
     __nv_bfloat16* out = xt + (size_t)(digits ? 4 * m : m) * K + (size_t)b * 1024;
-    if (VEC)
-        store_rotated_vec(v, out, K, digits, lane);
-    else
-        store_rotated(v, out, K, digits, [lane](int r) { return 32 * r + lane; });
+    store_rotated(v, out, K, digits, [lane](int r) { return 32 * r + lane; });
 }
 
 }  // namespace
