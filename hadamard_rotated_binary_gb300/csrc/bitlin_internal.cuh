@@ -112,7 +112,9 @@ struct PrefillParams {
     int M, N, K;
     int num_sms;            // for the split-K choice
     long long wait_budget_ns;
-    int tiles_x, tiles;     // set by the launcher (persistent grid): tiles along N, tiles in all
+    // Set by the launcher (persistent grid): tiles along N, and the launch's
+    // tiles: tiles tile_base .. tile_base + tiles - 1 of the row-major tile grid.
+    int tiles_x, tiles, tile_base;
 };
 
 }  // namespace bitlin_impl

@@ -146,8 +146,8 @@ __global__ void __launch_bounds__(kThreads, OCC)
     const int gbase = (int)((long long)Gall * blockIdx.z / gridDim.z);
     const int G = (int)((long long)Gall * (blockIdx.z + 1) / gridDim.z) - gbase;
     const long long budget = p.wait_budget_ns;
-    // The CTA's tiles: its grid tile, or (persistent) tiles blockIdx.x,
-    // blockIdx.x + gridDim.x, ... of the tiles_x-wide grid of tiles.  Every
+    // The CTA's tiles: its grid tile, or (persistent) tiles tile_base +
+    // blockIdx.x, + gridDim.x, ... of the tiles_x-wide grid of tiles.  Every
     // role runs one group counter gg over all of them (tile gg / G, K-group
     // gg % G), so stages, barrier phases and accumulator buffers carry on from
     // one tile to the next.
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, OCC)
     const int GT = ntiles * G;
     auto tile_xy = [&](int ti, int& tn0, int& tb0) {
         if (PERSIST) {
-            const int t = (int)blockIdx.x + ti * (int)gridDim.x;
+            const int t = p.tile_base + (int)blockIdx.x + ti * (int)gridDim.x;
             const int ty = t / p.tiles_x;
             tn0 = (t - ty * p.tiles_x) * kPrefillRows;
             tb0 = ty * BN;
@@ -437,16 +437,36 @@ __global__ void __launch_bounds__(kThreads, OCC)
     if (threadIdx.x == 0 && bar->abort) atomicExch(p.dev_error, kDevErrTimeout);
 }
 
+// PERSIST: the launch covers tiles tile_base .. tile_base + tile_count - 1 of
+// the row-major tile grid (tile_count 0: all of them).
 template <int BN, bool EXACT, int OCC = 1, bool PERSIST = false>
 cudaError_t launch(const PrefillParams& p, const void* tmap, const void* tmap_bits, int stall_test,
-                   cudaStream_t s)
+                   cudaStream_t s, int tile_base = 0, int tile_count = 0)
 {
-    // Once per device (the attribute applies to the current device).
+    // Once per device (the attribute applies to the current device): the shared
+    // memory size, and how many clusters of each split-K size can be resident
+    // at once (max_clusters[dev][s]).
     static PerDeviceOnce once;
+    static int max_clusters[kMaxDevices][kMaxSplits + 1];
     int dev = 0;
-    cudaError_t ce = once.run(&dev, [](int) {
-        return cudaFuncSetAttribute(bitlin_tc_gemm<BN, EXACT, OCC, PERSIST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    smem_bytes<BN, OCC>());
+    cudaError_t ce = once.run(&dev, [](int d) {
+        cudaError_t e = cudaFuncSetAttribute(bitlin_tc_gemm<BN, EXACT, OCC, PERSIST>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<BN, OCC>());
+        for (int z = 2; z <= kMaxSplits && e == cudaSuccess; ++z) {
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 1;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = z;
+            cudaLaunchConfig_t c = {};
+            c.gridDim = dim3(1, 1, z);
+            c.blockDim = dim3(kThreads);
+            c.dynamicSmemBytes = smem_bytes<BN, OCC>();
+            c.attrs = at;
+            c.numAttrs = 1;
+            e = cudaOccupancyMaxActiveClusters(&max_clusters[d][z], bitlin_tc_gemm<BN, EXACT, OCC, PERSIST>, &c);
+        }
+        return e;
     });
     if (ce != cudaSuccess) return ce;
     const int rows_b = EXACT ? 4 * p.M : p.M;
@@ -455,11 +475,15 @@ cudaError_t launch(const PrefillParams& p, const void* tmap, const void* tmap_bi
     // short-N matrices at small M, e.g. 17408 -> 5120): as many splits as
     // still fit one wave, at most 8 and at least 8 K-groups each.
     int splits = 1;
-    const int tiles = gx * gy, Gall = p.K / 128;
+    const int tiles = PERSIST && tile_count > 0 ? tile_count : gx * gy, Gall = p.K / 128;
     if (2 * tiles < OCC * p.num_sms) {
         splits = OCC * p.num_sms / tiles;
         if (splits > kMaxSplits) splits = kMaxSplits;
         if (splits > Gall / 8) splits = Gall / 8;
+        // All tiles' clusters must be resident at once: one cluster more than
+        // fits runs as a second wave (on 152 SMs at about 200 KB of shared
+        // memory a CTA, 46 clusters of 3 fit, not 48; 28 of 5).
+        while (splits > 1 && max_clusters[dev][splits] < tiles) --splits;
         if (splits < 1) splits = 1;
     }
     const CUtensorMap tb = *static_cast<const CUtensorMap*>(tmap);
@@ -475,7 +499,8 @@ cudaError_t launch(const PrefillParams& p, const void* tmap, const void* tmap_bi
     PrefillParams q = p;
     q.tiles_x = gx;
     q.tiles = tiles;
-    cfg.gridDim = PERSIST ? dim3(tiles < OCC * p.num_sms ? tiles : OCC * p.num_sms) : dim3(gx, gy, splits);
+    q.tile_base = PERSIST ? tile_base : 0;
+    cfg.gridDim = PERSIST ? dim3(tiles < OCC * p.num_sms ? tiles : OCC * p.num_sms, 1, splits) : dim3(gx, gy, splits);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem_bytes<BN, OCC>();
     cfg.stream = s;
@@ -500,7 +525,23 @@ cudaError_t bitlin_launch_prefill(const PrefillParams& p, const void* tmap, cons
     // follow the last groups of the previous one without a CTA start in
     // between (prefill 173.5 -> 168.8 us, gate_up at M = 1024 317.8 -> 306.5).
     const int tiles = ((p.N + kPrefillRows - 1) / kPrefillRows) * ((p.M + kPrefillTokens - 1) / kPrefillTokens);
-    if (tiles > p.num_sms) return launch<kPrefillTokens, false, 1, true>(p, tmap, tmap_bits, stall_test, s);
+    if (tiles > p.num_sms) {
+        // The tiles past the last full wave would run on that many SMs while
+        // the others idle.  When they fill less than half of the SMs, they
+        // get a launch of their own, each split along K over a cluster (the
+        // split-K finish), so that every SM takes part: prefill 165.5 ->
+        // 158.5 us (1064 + 24 tiles, split 5), the MLP block at M = 1024
+        // 542.6 -> 492.5 (gate_up 2128 + 48 tiles, split 2; down 304 + 16,
+        // split 8).  The tail waits for the first launch (programmatic
+        // dependent launch), whose CTAs all end at about the same time.
+        const int full = tiles / p.num_sms * p.num_sms, rem = tiles - full;
+        if (rem > 0 && 2 * rem < p.num_sms) {
+            const cudaError_t e = launch<kPrefillTokens, false, 1, true>(p, tmap, tmap_bits, stall_test, s, 0, full);
+            if (e != cudaSuccess) return e;
+            return launch<kPrefillTokens, false, 1, true>(p, tmap, tmap_bits, stall_test, s, full, rem);
+        }
+        return launch<kPrefillTokens, false, 1, true>(p, tmap, tmap_bits, stall_test, s);
+    }
     return launch<kPrefillTokens, false>(p, tmap, tmap_bits, stall_test, s);
 }
 

@@ -149,10 +149,14 @@ def test_prefill_full_size_every_output(hrb):
 
 
 @pytest.mark.parametrize("N,K,M,perm", [(300, 2048, 65, 0), (129, 1024, 130, 0), (256, 6144, 128, 1),
-                                        (1000, 3072, 200, 0), (1000, 2048, 2600, 0), (5000, 6144, 520, 1)])
+                                        (1000, 3072, 200, 0), (1000, 2048, 2600, 0), (5000, 6144, 520, 1),
+                                        (2048, 1024, 1900, 0)])
 def test_prefill_ragged(hrb, N, K, M, perm):
-    """Ragged N and M on the bf16 tensor path, every output; the last two cases have more tiles
-    than SMs (8 x 21 and 40 x 5), so they run on the persistent grid with ragged edge tiles."""
+    """Ragged N and M on the bf16 tensor path, every output.  The last three cases have more
+    tiles than SMs (8 x 21, 40 x 5 and 16 x 15), so they run on the persistent grid with ragged
+    edge tiles.  On 152 SMs the first two leave 16 and 48 tiles past the last full wave, which
+    run as a second, split-K launch; the third leaves 88 (more than half the SMs), which stay
+    in the persistent grid."""
     seed = 7 + N + K + M
     bits = synth.random_bits(seed, N, K)
     scales = synth.random_scales(seed, N, K, 0.005, 0.03)
