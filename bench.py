@@ -169,10 +169,11 @@ def roofline(w: synth.Workload, s_per_step: float, peaks: dict, peak_kind: str, 
     Decode: HBM-bound, algorithmic bytes per call over the step time (one GEMV per step; with
     kernels = 2 the step also holds the small split-K sum, which the GEMV overlaps through
     programmatic dependent launch, so the fraction is a lower bound).  Tensor paths: the tcgen05
-    GEMM, 2*M*N*K bf16 MMA flops per launch (the exact path multiplies three bf16 digit columns per
-    token, 3x that) over the step time, which also holds the small rotation kernel, so the
-    fraction is a lower bound; peak = the measured burst bf16 GEMM rate (the timed loop lasts
-    milliseconds)."""
+    GEMM (one launch, or two when its tiles past the last full wave of SMs run as a split-K launch
+    of their own), 2*M*N*K bf16 MMA flops per call (the exact path multiplies three bf16 digit
+    columns per token, 3x that) over the step time, which also holds the small rotation kernel,
+    so the fraction is a lower bound; peak = the measured burst bf16 GEMM rate (the timed loop
+    lasts milliseconds); traffic = DRAM bytes of the call's GEMM launches together."""
     if path == 1:
         kernel = "bitlin_decode_gemv" + (" + bitlin_decode_reduce" if kernels == 2 else "")
         achieved = w.algorithmic_bytes() / s_per_step / 1e9
@@ -582,7 +583,8 @@ def run_op(args, ws, rank, local, pg):
         algo = M * (row + 4 + 4 * K) + 4 * K
         roof = {"bound": "hbm", "achieved": algo / s_step / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "kernel": "bitlin_embed_rows", "bytes_per_launch": algo}
-        roof.update({"frac": roof["achieved"] / roof["peak"], "peak_kind": peak_kind, "traffic": None})
+        roof.update({"frac": roof["achieved"] / roof["peak"], "peak_kind": peak_kind,
+                     "traffic": traffic_record("bitlin_embed_rows", "embed", M)})
         metric, config = EMBED_METRIC, {"workload": "embed", "M": M, "N": N, "K": K,
                                         "l2": f"table of {N * row / 1e6:.0f} MB > L2; {nsets} id sets of random rows"}
         launches, wgb = 1, M * row / s_step / 1e9

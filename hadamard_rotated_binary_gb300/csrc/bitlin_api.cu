@@ -361,7 +361,9 @@ bitlin_status bitlin_plan(bitlin_t h, int M, int* path, int* kernels)
     if (!h || !path || !kernels || M < 1) return BITLIN_EINVAL;
     *path = choose_path(h, M);
     if (*path != BITLIN_PATH_DECODE) {
-        *kernels = 2;  // the rotation into bf16, then the tensor-core GEMM
+        // the rotation into bf16, then the tensor-core GEMM (bf16 path: two
+        // launches when the tiles past the last full wave are split over K)
+        *kernels = 1 + (*path == BITLIN_PATH_PREFILL ? bitlin_prefill_gemm_launches(M, h->N, h->num_sms) : 1);
         return BITLIN_OK;
     }
     return from_cuda(h, bitlin_decode_kernels(decode_params(h, nullptr, M, nullptr, 0), h->num_sms, kernels));

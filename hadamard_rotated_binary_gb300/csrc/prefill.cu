@@ -517,6 +517,26 @@ int bitlin_tc_tile_width(int M, int exact)
     return 4 * M <= 64 ? 64 : 128;
 }
 
+namespace {
+
+// Tiles of the bf16 path, and how many of them come after the last full wave
+// of num_sms when those get a launch of their own (0: one launch).
+int prefill_tail(int M, int N, int num_sms, int* tiles)
+{
+    *tiles = ((N + kPrefillRows - 1) / kPrefillRows) * ((M + kPrefillTokens - 1) / kPrefillTokens);
+    if (*tiles <= num_sms) return 0;
+    const int rem = *tiles - *tiles / num_sms * num_sms;
+    return 2 * rem < num_sms ? rem : 0;
+}
+
+}  // namespace
+
+int bitlin_prefill_gemm_launches(int M, int N, int num_sms)
+{
+    int tiles = 0;
+    return prefill_tail(M, N, num_sms, &tiles) > 0 ? 2 : 1;
+}
+
 cudaError_t bitlin_launch_prefill(const PrefillParams& p, const void* tmap, const void* tmap_bits,
                                   int stall_test, cudaStream_t s)
 {
@@ -524,7 +544,8 @@ cudaError_t bitlin_launch_prefill(const PrefillParams& p, const void* tmap, cons
     // need more than one wave: the next tile's loads, bits and expansion then
     // follow the last groups of the previous one without a CTA start in
     // between (prefill 173.5 -> 168.8 us, gate_up at M = 1024 317.8 -> 306.5).
-    const int tiles = ((p.N + kPrefillRows - 1) / kPrefillRows) * ((p.M + kPrefillTokens - 1) / kPrefillTokens);
+    int tiles = 0;
+    const int rem = prefill_tail(p.M, p.N, p.num_sms, &tiles);
     if (tiles > p.num_sms) {
         // The tiles past the last full wave would run on that many SMs while
         // the others idle.  When they fill less than half of the SMs, they
@@ -534,8 +555,8 @@ cudaError_t bitlin_launch_prefill(const PrefillParams& p, const void* tmap, cons
         // 542.6 -> 492.5 (gate_up 2128 + 48 tiles, split 2; down 304 + 16,
         // split 8).  The tail waits for the first launch (programmatic
         // dependent launch), whose CTAs all end at about the same time.
-        const int full = tiles / p.num_sms * p.num_sms, rem = tiles - full;
-        if (rem > 0 && 2 * rem < p.num_sms) {
+        if (rem > 0) {
+            const int full = tiles - rem;
             const cudaError_t e = launch<kPrefillTokens, false, 1, true>(p, tmap, tmap_bits, stall_test, s, 0, full);
             if (e != cudaSuccess) return e;
             return launch<kPrefillTokens, false, 1, true>(p, tmap, tmap_bits, stall_test, s, full, rem);

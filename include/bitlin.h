@@ -277,8 +277,10 @@ bitlin_status bitlin_set_path(bitlin_t h, int path);
  * The plan of a bitlin_forward call with M tokens on this handle, without
  * running it: *path = the BITLIN_PATH_* it takes (never AUTO), *kernels = the
  * kernels it launches (decode: 1 when the split-K sums inside a thread-block
- * cluster, 2 when a second kernel sums the partials; tensor paths: 2, the
- * rotation and the GEMM).  The first call may set up the decode kernels'
+ * cluster, 2 when a second kernel sums the partials; tensor paths: the
+ * rotation and the GEMM, 2, or 3 on the bf16 path when the GEMM's tiles past
+ * its last full wave of SMs run as a second, split-K launch).  The first call
+ * may set up the decode kernels'
  * attributes on the current device.  Errors: BITLIN_EINVAL (NULL argument,
  * M < 1), BITLIN_ECUDA.
  */

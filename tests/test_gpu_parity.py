@@ -354,10 +354,17 @@ def test_auto_path_choice(hrb):
 def test_plan_reports_path_and_kernels(hrb):
     """bitlin_plan: the path of each M range, one kernel for the cluster split-K (10 slices at
     K = 5120), two (GEMV + sum) for 34 slices at K = 17408 and for 128 at K = 65536, two
-    (rotation + GEMM) on the tensor paths; a forced path is reported as forced."""
+    (rotation + GEMM) on the tensor paths, three on the bf16 path when the GEMM's tiles past its
+    last full wave (fewer than half the SMs) run as a split-K launch of their own; a forced path
+    is reported as forced."""
     gate = make_layer(hrb, *inputs("ffn_gate", 1)[1:4], 0)
     down = make_layer(hrb, *inputs("ffn_down", 1)[1:4], 0)
     assert [gate.plan(m) for m in (1, 2, 6, 7, 63, 64)] == [(1, 1), (1, 1), (1, 1), (3, 2), (3, 2), (2, 2)]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for m in (256, 1024, 1900):
+        tiles = 136 * -(-m // 128)  # 17408 rows / 128 per tile, 128 tokens per tile
+        tail = tiles > sms and 0 < 2 * (tiles % sms) < sms
+        assert gate.plan(m) == (2, 3 if tail else 2), (m, sms)
     assert down.plan(1) == (1, 2)
     wide = make_layer(hrb, synth.random_bits(3, 64, 65536), synth.random_scales(3, 64, 65536, 0.005, 0.03),
                       synth.random_signs(3, 65536), 0)
