@@ -482,8 +482,11 @@ cudaError_t launch(const PrefillParams& p, const void* tmap, const void* tmap_bi
         if (splits > Gall / 8) splits = Gall / 8;
         // All tiles' clusters must be resident at once: one cluster more than
         // fits runs as a second wave (on 152 SMs at about 200 KB of shared
-        // memory a CTA, 46 clusters of 3 fit, not 48; 28 of 5).
-        while (splits > 1 && max_clusters[dev][splits] < tiles) --splits;
+        // memory a CTA, 46 clusters of 3 fit, not 48; 28 of 5).  The query
+        // reports the same counts for the two-CTAs-per-SM instance, which
+        // holds twice as many (80 clusters of 3 run as one wave there: attn_qkv
+        // at M = 16 19.7 us, 31.4 with the split cut to 1), hence * OCC.
+        while (splits > 1 && OCC * max_clusters[dev][splits] < tiles) --splits;
         if (splits < 1) splits = 1;
     }
     const CUtensorMap tb = *static_cast<const CUtensorMap*>(tmap);
