@@ -194,7 +194,7 @@ cudaError_t bitlin_launch_prefill(const bitlin_impl::PrefillParams& p, const voi
                                   const void* tmap_bits, int stall_test, cudaStream_t s);
 cudaError_t bitlin_launch_tc_exact(const bitlin_impl::PrefillParams& p, const void* tmap,
                                    const void* tmap_bits, int stall_test, cudaStream_t s);
-// Rows of B per tensor-core tile: 128 tokens (prefill) or 64/128/192/256 digit rows (exact).
+// Rows of B per tensor-core tile: 64 or 128 tokens (bf16 path) or 64/128 digit rows (exact).
 int bitlin_tc_tile_width(int M, int exact);
 // GEMM launches of a bf16 tensor-path call: 2 when the tiles past the last
 // full wave get a split-K launch of their own, else 1.

@@ -8,7 +8,8 @@
 //
 // Two modes of the same kernel:
 //  * prefill (M >= 64): the B operand is xt rounded to bf16, one row per
-//    token; CTA tile = 128 weight rows x BN tokens, tokens split over grid.y.
+//    token; CTA tile = 128 weight rows x BN tokens (BN = 64 up to 64 tokens,
+//    else 128), tokens split over grid.y.
 //  * exact (2 <= M < 64): the B operand holds, for token m, rows 4m..4m+2 =
 //    the three bf16 digits hi, mid, lo of xt (hi = bf16(xt), mid =
 //    bf16(xt - hi), lo = bf16(xt - hi - mid): together the f32 value) and row
@@ -132,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, OCC)
     constexpr int kHalf = BN / 2;                    // columns per epilogue warp
     constexpr int kChunks = kHalf / 32;              // tcgen05.ld x32 loads per group
     constexpr int kAcc = EXACT ? kHalf / 4 : kHalf;  // accumulators per epilogue thread
+    constexpr bool kNarrow = !EXACT && OCC == 2;     // 16-column reads: 32 accumulators in 64 registers
     static_assert(BN % 64 == 0 && BN <= 128, "tile width");
 
     extern __shared__ unsigned char smem_raw[];
@@ -357,6 +359,24 @@ __global__ void __launch_bounds__(kThreads, OCC)
                 ptx::tc_fence_after();
                 const uint32_t taddr =
                     tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN + kHalf * half);
+                if (kNarrow) {
+                    // 16-column reads (the bf16 half-SM instance's 64 registers)
+#pragma unroll
+                    for (int c = 0; c < kHalf / 16; ++c) {
+                        float v[16];
+                        ptx::tmem_ld16(taddr + 16 * c, v);
+                        ptx::tmem_wait_ld();
+                        if (c == kHalf / 16 - 1) {
+                            ptx::tc_fence_before();
+                            ptx::mbar_arrive(&bar->tempty[buf]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; j += 2) {
+                            acc2[(16 * c + j) / 2].x = fmaf(s, v[j], acc2[(16 * c + j) / 2].x);
+                            acc2[(16 * c + j) / 2].y = fmaf(s, v[j + 1], acc2[(16 * c + j) / 2].y);
+                        }
+                    }
+                } else
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c) {
                     float v[32];
@@ -518,7 +538,7 @@ cudaError_t launch(const PrefillParams& p, const void* tmap, const void* tmap_bi
 
 int bitlin_tc_tile_width(int M, int exact)
 {
-    if (!exact) return kPrefillTokens;
+    if (!exact) return M <= 64 ? 64 : kPrefillTokens;
     return 4 * M <= 64 ? 64 : 128;
 }
 
@@ -538,6 +558,7 @@ int prefill_tail(int M, int N, int num_sms, int* tiles)
 
 int bitlin_prefill_gemm_launches(int M, int N, int num_sms)
 {
+    if (bitlin_tc_tile_width(M, 0) == 64) return 1;
     int tiles = 0;
     return prefill_tail(M, N, num_sms, &tiles) > 0 ? 2 : 1;
 }
@@ -549,6 +570,17 @@ cudaError_t bitlin_launch_prefill(const PrefillParams& p, const void* tmap, cons
     // need more than one wave: the next tile's loads, bits and expansion then
     // follow the last groups of the previous one without a CTA start in
     // between (prefill 173.5 -> 168.8 us, gate_up at M = 1024 317.8 -> 306.5).
+    if (bitlin_tc_tile_width(p.M, 0) == 64) {
+        // At most 64 tokens: 64-wide tiles (the exact path's shape) instead of
+        // 128-wide ones half filled with zeros; two CTAs per SM when the tiles
+        // fill every SM (gate_up at M = 64 46.8 -> 34.7 us, the LM head 257.8 ->
+        // 191.5, ffn_down 33.3 -> 28.0, ffn_gate 25.0 -> 23.5, attn_qkv 22.9 ->
+        // 20.6; two per SM from half the SMs, as the exact path does, measured
+        // slower here: ffn_gate 26.7, attn_q 25.5).
+        const int tiles = (p.N + kPrefillRows - 1) / kPrefillRows;
+        if (tiles >= p.num_sms) return launch<64, false, 2>(p, tmap, tmap_bits, stall_test, s);
+        return launch<64, false>(p, tmap, tmap_bits, stall_test, s);
+    }
     int tiles = 0;
     const int rem = prefill_tail(p.M, p.N, p.num_sms, &tiles);
     if (tiles > p.num_sms) {

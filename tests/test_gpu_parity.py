@@ -169,6 +169,30 @@ def test_prefill_ragged(hrb, N, K, M, perm):
     assert max_rel_l2(y, ref16) <= BF16_DIAG_TOL
 
 
+@pytest.mark.parametrize("N,K,M", [(1000, 2048, 33), (20000, 1024, 50), (5120, 17408, 64), (300, 1024, 1)])
+def test_prefill_narrow_tiles(hrb, N, K, M):
+    """The bf16 path at most 64 tokens runs 64-token tiles: one CTA per SM with split-K for
+    few tiles (8 tiles split 2; 40 tiles split 3 at K = 17,408), two per SM when the tiles fill
+    every SM (157 tiles on 152 SMs), ragged N and M; the path is forced where M alone would
+    pick the decode GEMV.  Every output (a sample of rows at K = 17,408) within 1e-2, and
+    within the bf16 diagnostic."""
+    seed = 13 + N + K + M
+    bits = synth.random_bits(seed, N, K)
+    scales = synth.random_scales(seed, N, K, 0.005, 0.03)
+    signs = synth.random_signs(seed, K)
+    x = synth.random_x(seed, M, K)
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    layer.set_path(hrb.PATH_PREFILL)
+    assert layer.plan(M) == (hrb.PATH_PREFILL, 2)  # the rotation and one GEMM launch
+    y = run(layer, x)
+    rows = synth.sample_rows(seed, N, 320) if K > 8192 else None
+    ref = oracle.forward(bits, scales, signs, 0, x, rows)
+    yy = y[:, rows] if rows is not None else y
+    assert max_rel_l2(yy, ref) <= PREFILL_TOL
+    ref16 = oracle.forward(bits, scales, signs, 0, x, rows, round_bf16=True)
+    assert max_rel_l2(yy, ref16) <= BF16_DIAG_TOL
+
+
 # ------------------------------------------------------------------ edge cases
 
 @pytest.mark.parametrize("N,K,M", [(1, 1024, 1), (100, 1024, 1), (31, 2048, 3), (1000, 3072, 5),
