@@ -515,6 +515,27 @@ def test_argmax_consecutive_calls_and_nan(hrb):
     assert layer.get_error() == 0
 
 
+def test_lm_head_bf16_narrow_tiles_m64(hrb):
+    """The vocabulary matrix at M = 64 on the bf16 path: 1940 tiles of 64 tokens, two CTAs per
+    SM over several waves; a seeded sample of rows within 1e-2 and the bf16 diagnostic, and the
+    ids picked by the separate argmax kernel equal to the argmax of the scores."""
+    bits, scales, signs, seed = _lm_head()
+    x = synth.random_x(seed + 1, 64, 5120)
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    assert layer.plan(64) == (hrb.PATH_PREFILL, 2)
+    logits = torch.empty((64, bits.shape[0]), dtype=torch.float32, device="cuda")
+    ids = layer.argmax(torch.from_numpy(x).cuda(), logits=logits).cpu().numpy()
+    torch.cuda.synchronize()
+    assert layer.get_error() == 0
+    lg = logits.cpu().numpy()
+    rows = synth.sample_rows(seed, bits.shape[0], 512)
+    ref = oracle.forward(bits, scales, signs, 0, x, rows)
+    assert max_rel_l2(lg[:, rows].astype(np.float64), ref) <= PREFILL_TOL
+    ref16 = oracle.forward(bits, scales, signs, 0, x, rows, round_bf16=True)
+    assert max_rel_l2(lg[:, rows].astype(np.float64), ref16) <= BF16_DIAG_TOL
+    assert np.array_equal(ids, np.argmax(lg, axis=1))
+
+
 # ------------------------------------------------------------------ embedding (inverse rotation)
 
 @pytest.mark.parametrize("name,ids", [("tiny", [0, 255, 17, 17, 128]), ("ffn_down", [0, 5119, 1234]),
