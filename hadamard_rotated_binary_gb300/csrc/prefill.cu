@@ -566,10 +566,6 @@ int bitlin_prefill_gemm_launches(int M, int N, int num_sms)
 cudaError_t bitlin_launch_prefill(const PrefillParams& p, const void* tmap, const void* tmap_bits,
                                   int stall_test, cudaStream_t s)
 {
-    // A persistent grid (one CTA per SM looping over the tiles) when the tiles
-    // need more than one wave: the next tile's loads, bits and expansion then
-    // follow the last groups of the previous one without a CTA start in
-    // between (prefill 173.5 -> 168.8 us, gate_up at M = 1024 317.8 -> 306.5).
     if (bitlin_tc_tile_width(p.M, 0) == 64) {
         // At most 64 tokens: 64-wide tiles (the exact path's shape) instead of
         // 128-wide ones half filled with zeros; two CTAs per SM when the tiles
@@ -581,6 +577,10 @@ cudaError_t bitlin_launch_prefill(const PrefillParams& p, const void* tmap, cons
         if (tiles >= p.num_sms) return launch<64, false, 2>(p, tmap, tmap_bits, stall_test, s);
         return launch<64, false>(p, tmap, tmap_bits, stall_test, s);
     }
+    // A persistent grid (one CTA per SM looping over the tiles) when the tiles
+    // need more than one wave: the next tile's loads, bits and expansion then
+    // follow the last groups of the previous one without a CTA start in
+    // between (prefill 173.5 -> 168.8 us, gate_up at M = 1024 317.8 -> 306.5).
     int tiles = 0;
     const int rem = prefill_tail(p.M, p.N, p.num_sms, &tiles);
     if (tiles > p.num_sms) {
