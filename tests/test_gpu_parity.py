@@ -106,10 +106,13 @@ def test_gate_up_decode_sweep(hrb, M):
     assert max_rel_l2(y, ref) <= DECODE_TOL
 
 
-@pytest.mark.parametrize("name,M", [("attn_qkv", 4), ("attn_gate", 16), ("attn_q", 8), ("attn_kv", 3),
-                                    ("attn_output", 5)])
+@pytest.mark.parametrize("name,M", [("attn_qkv", 4), ("attn_qkv", 16), ("attn_gate", 16), ("attn_q", 8),
+                                    ("attn_kv", 3), ("attn_output", 5)])
 def test_attention_shapes_small_batch(hrb, name, M):
-    """The attention-side folded shapes at small M (decode GEMV to M = 6, exact tensor path above), sampled rows."""
+    """The attention-side folded shapes at small M (decode GEMV to M = 6, exact tensor path above), sampled rows.
+    On 152 SMs the exact cases run split-K over clusters: attn_qkv at M = 16 two CTAs per SM split 3,
+    attn_q at M = 8 two per SM split 2, attn_gate at M = 16 one per SM split 2 (the resident-cluster
+    limit cuts 3 to 2)."""
     w, bits, scales, signs, x = inputs(name, M)
     y = run(make_layer(hrb, bits, scales, signs, w.perm), x)
     rows = synth.sample_rows(w.seed, w.N, 768)
@@ -167,6 +170,26 @@ def test_prefill_ragged(hrb, N, K, M, perm):
     assert max_rel_l2(y, ref) <= PREFILL_TOL
     ref16 = oracle.forward(bits, scales, signs, perm, x, round_bf16=True)
     assert max_rel_l2(y, ref16) <= BF16_DIAG_TOL
+
+
+def test_prefill_whole_waves_no_tail(hrb):
+    """Tiles an exact multiple of the SMs (2 waves of 128-token tiles): the persistent grid with
+    no split tail launch.  Sampled rows within 1e-2 and the bf16 diagnostic."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    N, K, M = sms * 128, 1024, 256
+    seed = 17
+    bits = synth.random_bits(seed, N, K)
+    scales = synth.random_scales(seed, N, K, 0.005, 0.03)
+    signs = synth.random_signs(seed, K)
+    x = synth.random_x(seed, M, K)
+    layer = make_layer(hrb, bits, scales, signs, 0)
+    assert layer.plan(M) == (hrb.PATH_PREFILL, 2)
+    y = run(layer, x)
+    rows = synth.sample_rows(seed, N, 512)
+    ref = oracle.forward(bits, scales, signs, 0, x, rows)
+    assert max_rel_l2(y[:, rows], ref) <= PREFILL_TOL
+    ref16 = oracle.forward(bits, scales, signs, 0, x, rows, round_bf16=True)
+    assert max_rel_l2(y[:, rows], ref16) <= BF16_DIAG_TOL
 
 
 @pytest.mark.parametrize("N,K,M", [(1000, 2048, 33), (20000, 1024, 50), (5120, 17408, 64), (300, 1024, 1)])
