@@ -457,6 +457,28 @@ def test_mlp_block_bf16_path_and_forced_paths(hrb):
     assert max_rel_l2(y.cpu().numpy().astype(np.float64), ref) <= DECODE_TOL
 
 
+def test_mlp_block_bf16_path_persistent_grids(hrb):
+    """1280 tokens through a 2048 -> 2 x 1024 -> 2048 block on the bf16 tensor path: both
+    products run persistent grids of more than one wave (gate_up 16 x 10 tiles, down 16 x 10),
+    the down projection's rotation with SiLU(gate) * up; within 1e-2 of the oracle on sampled
+    rows, and the same bits from a second call."""
+    F, H, M = 1024, 2048, 1280
+    gu, dn, lgu, ldn = _mlp_pair(hrb, F, H, 77)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert -(-2 * F // 128) * -(-M // 128) > sms and -(-H // 128) * -(-M // 128) > sms
+    assert lgu.plan(M)[0] == ldn.plan(M)[0] == hrb.PATH_PREFILL
+    x = synth.random_x(78, M, H)
+    xd = torch.from_numpy(x).cuda()
+    y1 = hrb.mlp_forward(lgu, ldn, xd)
+    y2 = hrb.mlp_forward(lgu, ldn, xd)
+    torch.cuda.synchronize()
+    assert lgu.get_error() == 0 and ldn.get_error() == 0
+    assert torch.equal(y1, y2)
+    rows = synth.sample_rows(79, H, 192)
+    ref = oracle.mlp(gu, dn, x, rows)
+    assert max_rel_l2(y1.cpu().numpy()[:, rows].astype(np.float64), ref) <= PREFILL_TOL
+
+
 def test_mlp_block_rejects_mismatched_pair(hrb):
     gu, dn, lgu, ldn = _mlp_pair(hrb, 1024, 1024, 41)
     w, bits, scales, signs, _ = inputs("tiny")
