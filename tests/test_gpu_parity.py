@@ -60,6 +60,15 @@ def max_rel_l2(y, ref):
     return float((num / den).max())
 
 
+def rel_err(y, ref):
+    """max_rel_l2 per token row; with fewer than 32 outputs per token that norm is the error of a
+    handful of dot products, any of which can be near zero by cancellation, so there the norm is
+    taken over the tokens of each output instead (the transpose)."""
+    if y.shape[1] >= 32:
+        return max_rel_l2(y, ref)
+    return max_rel_l2(np.ascontiguousarray(y.T), np.ascontiguousarray(ref.T))
+
+
 def inputs(name, M=None):
     w = synth.workload(name, M)
     return (w,) + synth.make_inputs(w)
@@ -153,13 +162,14 @@ def test_prefill_full_size_every_output(hrb):
 
 @pytest.mark.parametrize("N,K,M,perm", [(300, 2048, 65, 0), (129, 1024, 130, 0), (256, 6144, 128, 1),
                                         (1000, 3072, 200, 0), (1000, 2048, 2600, 0), (5000, 6144, 520, 1),
-                                        (2048, 1024, 1900, 0)])
+                                        (2048, 1024, 1900, 0), (1, 1024, 65, 0), (100, 2048, 300, 0)])
 def test_prefill_ragged(hrb, N, K, M, perm):
-    """Ragged N and M on the bf16 tensor path, every output.  The last three cases have more
-    tiles than SMs (8 x 21, 40 x 5 and 16 x 15), so they run on the persistent grid with ragged
-    edge tiles.  On 152 SMs the first two leave 16 and 48 tiles past the last full wave, which
-    run as a second, split-K launch; the third leaves 88 (more than half the SMs), which stay
-    in the persistent grid."""
+    """Ragged N and M on the bf16 tensor path, every output.  Three cases have more tiles than
+    SMs (1000 x 2600: 8 x 21 tiles, 5000 x 520: 40 x 5, 2048 x 1900: 16 x 15), so they run on
+    the persistent grid with ragged edge tiles.  On 152 SMs the first two leave 16 and 48 tiles
+    past the last full wave, which run as a second, split-K launch; the third leaves 88 (more
+    than half the SMs), which stay in the persistent grid.  N = 1 and 100: fewer rows than one
+    128-row tile (the bits copy reads past N, the epilogue writes the rows that exist)."""
     seed = 7 + N + K + M
     bits = synth.random_bits(seed, N, K)
     scales = synth.random_scales(seed, N, K, 0.005, 0.03)
@@ -167,9 +177,9 @@ def test_prefill_ragged(hrb, N, K, M, perm):
     x = synth.random_x(seed, M, K)
     y = run(make_layer(hrb, bits, scales, signs, perm), x)
     ref = oracle.forward(bits, scales, signs, perm, x)
-    assert max_rel_l2(y, ref) <= PREFILL_TOL
+    assert rel_err(y, ref) <= PREFILL_TOL
     ref16 = oracle.forward(bits, scales, signs, perm, x, round_bf16=True)
-    assert max_rel_l2(y, ref16) <= BF16_DIAG_TOL
+    assert rel_err(y, ref16) <= BF16_DIAG_TOL
 
 
 def test_prefill_whole_waves_no_tail(hrb):
@@ -192,13 +202,14 @@ def test_prefill_whole_waves_no_tail(hrb):
     assert max_rel_l2(y[:, rows], ref16) <= BF16_DIAG_TOL
 
 
-@pytest.mark.parametrize("N,K,M", [(1000, 2048, 33), (20000, 1024, 50), (5120, 17408, 64), (300, 1024, 1)])
+@pytest.mark.parametrize("N,K,M", [(1000, 2048, 33), (20000, 1024, 50), (5120, 17408, 64), (300, 1024, 1),
+                                   (1, 2048, 64), (7, 1024, 20)])
 def test_prefill_narrow_tiles(hrb, N, K, M):
     """The bf16 path at most 64 tokens runs 64-token tiles: one CTA per SM with split-K for
     few tiles (8 tiles split 2; 40 tiles split 3 at K = 17,408), two per SM when the tiles fill
     every SM (157 tiles on 152 SMs), ragged N and M; the path is forced where M alone would
-    pick the decode GEMV.  Every output (a sample of rows at K = 17,408) within 1e-2, and
-    within the bf16 diagnostic."""
+    pick the decode GEMV; N = 1 and 7, fewer rows than one tile.  Every output (a sample of rows
+    at K = 17,408) within 1e-2, and within the bf16 diagnostic."""
     seed = 13 + N + K + M
     bits = synth.random_bits(seed, N, K)
     scales = synth.random_scales(seed, N, K, 0.005, 0.03)
@@ -211,9 +222,9 @@ def test_prefill_narrow_tiles(hrb, N, K, M):
     rows = synth.sample_rows(seed, N, 320) if K > 8192 else None
     ref = oracle.forward(bits, scales, signs, 0, x, rows)
     yy = y[:, rows] if rows is not None else y
-    assert max_rel_l2(yy, ref) <= PREFILL_TOL
+    assert rel_err(yy, ref) <= PREFILL_TOL
     ref16 = oracle.forward(bits, scales, signs, 0, x, rows, round_bf16=True)
-    assert max_rel_l2(yy, ref16) <= BF16_DIAG_TOL
+    assert rel_err(yy, ref16) <= BF16_DIAG_TOL
 
 
 # ------------------------------------------------------------------ edge cases
@@ -369,10 +380,13 @@ def test_rotation_with_unaligned_activations(hrb, M, perm):
 
 
 @pytest.mark.parametrize("M,N,K,perm", [(2, 256, 1024, 0), (16, 1000, 2048, 0), (17, 384, 6144, 1),
-                                        (40, 300, 3072, 0), (63, 129, 1024, 0), (100, 200, 1024, 0)])
+                                        (40, 300, 3072, 0), (63, 129, 1024, 0), (100, 200, 1024, 0),
+                                        (9, 1, 1024, 0), (16, 7, 2048, 0), (33, 100, 4096, 0)])
 def test_tc_exact_path_every_tile_width(hrb, M, N, K, perm):
-    """Activations split into three bf16 digits: f32-level results at both tile widths (64, 128) and
-    with the tokens spread over several tiles (M = 40, 63, 100)."""
+    """Activations split into three bf16 digits: f32-level results at both tile widths (64, 128),
+    with the tokens spread over several tiles (M = 40, 63, 100), and with fewer rows than one
+    128-row tile (N = 1, 7, 100: the bits copy reads past N, the epilogue writes the rows that
+    exist; split-K over 2 and 4 K-group ranges at K = 2048 and 4096)."""
     seed = 23 + M + N + K
     bits = synth.random_bits(seed, N, K)
     scales = synth.random_scales(seed, N, K, 0.005, 0.03)
@@ -381,9 +395,9 @@ def test_tc_exact_path_every_tile_width(hrb, M, N, K, perm):
     layer = make_layer(hrb, bits, scales, signs, perm)
     y = run(layer, x, path=hrb.PATH_TC_EXACT)
     ref = oracle.forward(bits, scales, signs, perm, x)
-    assert max_rel_l2(y, ref) <= DECODE_TOL
+    assert rel_err(y, ref) <= DECODE_TOL
     y_dec = run(layer, x, path=hrb.PATH_DECODE)
-    assert max_rel_l2(y_dec, ref) <= DECODE_TOL
+    assert rel_err(y_dec, ref) <= DECODE_TOL
 
 
 def test_auto_path_choice(hrb):
